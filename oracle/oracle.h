@@ -1,0 +1,73 @@
+/*
+ * oracle.h -- plain, slow, single-threaded CPU oracle for the MoE routing step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this library.  It shares no code with
+ * the CUDA path and the CUDA path never calls it.
+ *
+ * What it computes (per token row t, then over all rows):
+ *   s_e  = sigmoid(logit_e)            "a sigmoid router" (vLLM PR #59693, description)
+ *   b_e  = s_e + bias_e                "with correction bias"  (same passage)
+ *   group-limited top-k over b          "and grouped top-k"    (same passage)
+ *   weights = s of the chosen experts renormalised to `scale`, rounded to bf16
+ *   packed  = (id << 16) | bf16 weight bits
+ *                         (sglang PR #37, description: "packed (id << 16 | bf16 weight) ids")
+ *   optional rank-local relabel (same passage: the rank's experts become
+ *   0..count-1, any other expert in top-k slot k becomes count + k,
+ *   num_experts = round_up(count + top_k, 4))
+ *   histogram, exclusive-scan offsets and a stable (expert, token, slot) permutation
+ *                         (same passage: "the same (token, local expert, weight)
+ *                          entries reach the expert GEMMs in the same order")
+ * Constants of the Kimi-K3 instance (896 experts, top_k 16, 8 groups of 112,
+ * keep 4 groups, group score = sum of the top-2 biased scores, scale 2.5, ties to
+ * the lower id, bf16 weights) are arguments here.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - sigmoid evaluated in double and rounded once to float; b is a float add.
+ *   - slot order within a row: biased score descending, ties to the lower id.
+ *   - group ties: the lower group index is kept first.
+ *   - experts of dropped groups are excluded (never masked to 0).
+ *   - top-2 counts equal values with multiplicity.
+ *   - renormalisation: den = float sum of s over slots in slot order,
+ *     w = float(float(s / den) * scale), then bf16 round-to-nearest-even; no epsilon.
+ *   - perm holds the expanded index t*k + j; all T*k entries are included, so in
+ *     rank-local mode bins count..count+k-1 hold the other ranks' slots.
+ *   - logits and bias are finite.
+ */
+#ifndef MOE_ROUTE_ORACLE_H
+#define MOE_ROUTE_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_DT_F32 = 0, ORACLE_DT_BF16 = 1 };
+
+/* sigma(x) = 1 / (1 + e^-x) evaluated in double, rounded once to float. */
+float oracle_sigmoid(float x);
+
+/* float -> bfloat16 bits, round to nearest, ties to even (finite inputs). */
+uint16_t oracle_f32_to_bf16(float x);
+
+/* Number of expert bins of the routed problem: count > 0 ? round_up(count + k, 4) : E. */
+int oracle_num_experts(int E, int k, int local_offset, int local_count);
+
+/* Full routing step.  logits: [T, E] row-major, float (dtype 0) or bf16 bits (dtype 1).
+ * bias: [E].  Outputs: packed [T, k], counts [NE], offsets [NE + 1], perm [T * k],
+ * ids_global [T, k] (nullable) = the chosen global expert ids in slot order.
+ * Returns 0, or -1 for an invalid argument (same rules as the library). */
+int oracle_route(const void* logits, int dtype, const float* bias, int T, int E, int k,
+                 int n_group, int topk_group, float scale, int local_offset, int local_count,
+                 int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 int32_t* ids_global);
+
+/* Router contraction: logits[t][e] = sum_h hidden[t][h] * w[e][h], bf16 inputs,
+ * accumulated in double in index order; output double [T, E]. */
+void oracle_router_gemm(const uint16_t* hidden, const uint16_t* w, int T, int H, int E,
+                        double* logits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

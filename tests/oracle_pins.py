@@ -1,0 +1,393 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` function takes a loaded oracle library (ctypes) and raises
+AssertionError when the oracle disagrees with:
+  * the exact sigmoid (mpmath at 100 bits, rounded correctly to float32),
+  * torch's float32 -> bfloat16 conversion (library routine),
+  * a brute-force full sort of every row (group scores, group choice, top-k),
+  * numpy's stable argsort / bincount / cumsum for histogram, scan, permutation,
+  * closed forms (equal scores give weights 2.5/16 = 0x3E20 in bf16),
+  * exact rational renormalisation (fractions),
+  * invariants stated for the method (unique ids, ids inside kept groups,
+    counts summing to T*k, perm a permutation, weights summing to the scale,
+    rank-local ids unique, < count+k, round-tripping to the global ids),
+  * facts printed on the pages (num_experts 128 at EP8, router size).
+The same functions are run against deliberately broken copies of the oracle in
+test_oracle_mutations.py to show that each plausible mistake is caught.
+"""
+from __future__ import annotations
+
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+
+import gen
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# --------------------------------------------------------------------- helpers
+
+def exact_sigmoid_f32(x: float):
+    """(correctly rounded float32 of sigma(x), True if sigma(x) lies within 2^-44
+    relative of a float32 rounding midpoint), via mpmath at 120 bits."""
+    import mpmath
+    with mpmath.workprec(120):
+        v = 1 / (1 + mpmath.exp(-mpmath.mpf(float(x))))
+        f = np.float32(float(v))
+        best, bd = None, None
+        cands = (np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf)))
+        for c in cands:
+            d = abs(mpmath.mpf(float(c)) - v)
+            if bd is None or d < bd:
+                best, bd = c, d
+        # distance to the nearest midpoint between best and a neighbour
+        lo = mpmath.mpf(float(np.nextafter(best, np.float32(-np.inf))))
+        hi = mpmath.mpf(float(np.nextafter(best, np.float32(np.inf))))
+        b = mpmath.mpf(float(best))
+        dm = min(abs(v - (b + lo) / 2), abs(v - (b + hi) / 2))
+        near_mid = bool(dm <= abs(v) * mpmath.mpf(2) ** -44)
+        return np.float32(best), near_mid
+
+
+def lib_sigmoid(lib, x: np.ndarray) -> np.ndarray:
+    return np.array([lib.oracle_sigmoid(float(v)) for v in np.asarray(x, np.float32).ravel()],
+                    dtype=np.float32).reshape(np.shape(x))
+
+
+def logits_f32(cfg) -> np.ndarray:
+    if cfg["dtype"] == "f32":
+        return np.asarray(cfg["logits"], np.float32)
+    return gen.bf16_bits_to_f32(cfg["logits"])
+
+
+def brute_force_rows(x: np.ndarray, s: np.ndarray, bias: np.ndarray, G: int, Kg: int, k: int):
+    """Full-sort reference of the selection: returns (ids [T,k], kept groups [T,Kg])."""
+    T, E = x.shape
+    gsz = E // G
+    b = (s.astype(np.float32) + bias.astype(np.float32)[None, :]).astype(np.float32)
+    ids = np.zeros((T, k), dtype=np.int64)
+    kept_all = np.zeros((T, Kg), dtype=np.int64)
+    for t in range(T):
+        row = b[t]
+        gs = []
+        for g in range(G):
+            top2 = sorted((float(v) for v in row[g * gsz:(g + 1) * gsz]), reverse=True)[:2]
+            gs.append(np.float32(np.float32(top2[0]) + np.float32(top2[1])))
+        order = sorted(range(G), key=lambda g: (-float(gs[g]), g))
+        kept = sorted(order[:Kg])
+        cand = [e for e in range(E) if e // gsz in kept]
+        cand.sort(key=lambda e: (-float(row[e]), e))
+        ids[t] = cand[:k]
+        kept_all[t] = kept
+    return ids, kept_all
+
+
+def unpack(packed: np.ndarray):
+    p = packed.astype(np.int64) & 0xFFFFFFFF
+    return (p >> 16).astype(np.int64), (p & 0xFFFF).astype(np.uint16)
+
+
+def run(lib, cfg, off=None, cnt=None):
+    return oracle.route(cfg["logits"], cfg["dtype"], cfg["bias"], cfg["T"], cfg["E"], cfg["k"],
+                        cfg["G"], cfg["Kg"], cfg["scale"],
+                        cfg.get("off", 0) if off is None else off,
+                        cfg.get("cnt", 0) if cnt is None else cnt, lib=lib)
+
+
+def small_cfg(T, E, G, Kg, k, seed, levels=5, bias_levels=(0.0, 0.25, -0.25), dtype="f32",
+              scale=2.5):
+    """Tiny instance with many exact ties: logits on a small integer grid."""
+    r = gen.raw64(1000 + seed, T * E)
+    x = ((r % np.uint64(levels)).astype(np.int64) - levels // 2).astype(np.float32) * 0.5
+    rb = gen.raw64(2000 + seed, E)
+    bias = np.array(bias_levels, dtype=np.float32)[(rb % np.uint64(len(bias_levels))).astype(np.int64)]
+    logits = x.reshape(T, E)
+    if dtype == "bf16":
+        logits = gen.f32_to_bf16_bits(logits)
+    return dict(logits=logits, dtype=dtype, bias=bias, T=T, E=E, k=k, G=G, Kg=Kg, scale=scale,
+                off=0, cnt=0)
+
+
+# ------------------------------------------------------------------------ pins
+
+def pin_sigmoid_exact(lib, n_random: int = 4000):
+    """The oracle's sigmoid (double evaluation, one rounding to float) equals the
+    correctly rounded value on every finite bf16 input below 20 in magnitude, a
+    sparse sample beyond, and random float32 inputs -- except where sigma(x) lies
+    within 2^-44 of a float32 midpoint, where double rounding may pick either
+    neighbour; there it must be within one ulp.  sigma(0) = 0.5."""
+    assert lib.oracle_sigmoid(0.0) == 0.5
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    xs = gen.bf16_bits_to_f32(bits)
+    xs = xs[np.isfinite(xs)]
+    core = xs[(np.abs(xs) < 20.0)]
+    rest = xs[(np.abs(xs) >= 20.0)][::97]
+    rnd = gen.uniform_f32(77, n_random, -30.0, 30.0)
+    n_mid = 0
+    for x in np.concatenate([core, rest, rnd]):
+        got = np.float32(lib.oracle_sigmoid(float(x)))
+        want, near_mid = exact_sigmoid_f32(float(x))
+        if near_mid:
+            n_mid += 1
+            assert abs(float(got) - float(want)) <= float(np.spacing(want)), float(x)
+        else:
+            assert got == want, (float(x), float(got), float(want))
+    # the midpoint zone is a small set (tiny |x|, where sigma(x) ~ 1/2 + x/4)
+    assert n_mid < 400, n_mid
+
+
+def pin_sigmoid_symmetry(lib):
+    """sigma(-x) = 1 - sigma(x): checked in exact arithmetic within one ulp of each."""
+    xs = gen.uniform_f32(78, 2000, -12.0, 12.0)
+    for x in xs:
+        a = Fraction(float(lib.oracle_sigmoid(float(x))))
+        b = Fraction(float(lib.oracle_sigmoid(float(-x))))
+        ulp = Fraction(float(np.spacing(np.float32(max(a, b)))))
+        assert abs(a + b - 1) <= ulp, float(x)
+
+
+def pin_bf16_rounding(lib):
+    import torch
+    vals = np.concatenate([
+        gen.uniform_f32(79, 5000, -3.0, 3.0),
+        gen.normal_f32(80, 5000) * np.float32(1e-3),
+        # exact halfway cases between two bf16 values (ties to even)
+        gen.bf16_bits_to_f32(np.arange(0x3F00, 0x3F40, dtype=np.uint16)) *
+        np.float32(1.0 + 2.0 ** -8),
+        np.array([0.15625, 2.5, 1.0, 0.0, -0.0, 1e-30, 3.0e38], dtype=np.float32),
+    ]).astype(np.float32)
+    want = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([lib.oracle_f32_to_bf16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def pin_selection_brute_force(lib):
+    """Tiny shapes with many ties: ids and slot order equal a full sort per row."""
+    cases = [
+        (8, 2, 1, 2), (8, 2, 2, 3), (8, 4, 2, 2), (16, 4, 2, 4), (16, 8, 3, 4), (16, 1, 1, 4),
+        (32, 4, 2, 4), (32, 8, 4, 16), (32, 2, 1, 16), (64, 8, 4, 16), (64, 16, 5, 8),
+    ]
+    for i, (E, G, Kg, k) in enumerate(cases):
+        cfg = small_cfg(T=40, E=E, G=G, Kg=Kg, k=k, seed=i)
+        out = run(lib, cfg)
+        x = logits_f32(cfg)
+        ids_bf, _ = brute_force_rows(x, lib_sigmoid(lib, x), cfg["bias"], G, Kg, k)
+        assert np.array_equal(out["ids"], ids_bf), (E, G, Kg, k)
+        lid, _ = unpack(out["packed"])
+        assert np.array_equal(lid, ids_bf)
+
+
+def pin_selection_exhaustive(lib):
+    """E=8, 2 groups of 4, keep 1 group, top 2: every logit vector in {-1,0,1}^8."""
+    E, G, Kg, k = 8, 2, 1, 2
+    grid = np.array(np.meshgrid(*([np.array([-1.0, 0.0, 1.0], np.float32)] * E), indexing="ij"))
+    x = grid.reshape(E, -1).T.copy().astype(np.float32)
+    bias = np.array([0.0, 0.0, 0.25, -0.25, 0.0, 0.25, 0.0, -0.25], dtype=np.float32)
+    cfg = dict(logits=x, dtype="f32", bias=bias, T=x.shape[0], E=E, k=k, G=G, Kg=Kg, scale=2.5)
+    out = run(lib, cfg)
+    ids_bf, _ = brute_force_rows(x, lib_sigmoid(lib, x), bias, G, Kg, k)
+    assert np.array_equal(out["ids"], ids_bf)
+
+
+def pin_selection_kimi_shape(lib):
+    """Kimi shape (896, 8 groups, keep 4, top 16) on tie-heavy rows: full-sort reference."""
+    cfg = gen.cfg4(T=48, n_hot=12)
+    out = run(lib, cfg)
+    x = logits_f32(cfg)
+    ids_bf, kept = brute_force_rows(x, lib_sigmoid(lib, x), cfg["bias"], cfg["G"], cfg["Kg"],
+                                    cfg["k"])
+    assert np.array_equal(out["ids"], ids_bf)
+    cfg0 = gen.cfg0()
+    out0 = run(lib, cfg0)
+    x0 = logits_f32(cfg0)
+    ids0, _ = brute_force_rows(x0, lib_sigmoid(lib, x0), cfg0["bias"], 8, 4, 16)
+    assert np.array_equal(out0["ids"], ids0)
+
+
+def pin_plain_topk(lib):
+    """One group, keep it: the method reduces to plain top-k (numpy lexsort)."""
+    cfg = small_cfg(T=64, E=32, G=1, Kg=1, k=8, seed=91)
+    out = run(lib, cfg)
+    x = logits_f32(cfg)
+    b = (lib_sigmoid(lib, x) + cfg["bias"][None, :]).astype(np.float32)
+    for t in range(cfg["T"]):
+        order = np.lexsort((np.arange(32), -b[t].astype(np.float64)))
+        assert np.array_equal(out["ids"][t], order[:8])
+
+
+def pin_keep_all_groups_is_noop(lib):
+    """Keeping every group gives the same ids as a single group of all experts."""
+    base = small_cfg(T=64, E=64, G=8, Kg=8, k=16, seed=92)
+    a = run(lib, base)
+    one = dict(base, G=1, Kg=1)
+    b = run(lib, one)
+    assert np.array_equal(a["ids"], b["ids"])
+
+
+def pin_weights(lib):
+    """Weights: within one bf16 ulp of the exact rational s_j / sum(s) * scale; they sum
+    to the scale within 1e-2; equal scores give 2.5/16 = 0.15625 = bf16 0x3E20."""
+    for cfg in (gen.cfg0(), small_cfg(T=32, E=64, G=8, Kg=4, k=16, seed=93)):
+        out = run(lib, cfg)
+        x = logits_f32(cfg)
+        s = lib_sigmoid(lib, x)
+        _, wb = unpack(out["packed"])
+        w = gen.bf16_bits_to_f32(wb).astype(np.float64)
+        assert np.all(np.abs(w.sum(axis=1) - cfg["scale"]) <= 1e-2)
+        for t in range(cfg["T"]):
+            sel = [Fraction(float(s[t, e])) for e in out["ids"][t]]
+            den = sum(sel)
+            for j, sj in enumerate(sel):
+                exact = sj / den * Fraction(cfg["scale"])
+                ulp = Fraction(2) ** (math.frexp(float(exact))[1] - 8)
+                assert abs(Fraction(float(w[t, j])) - exact) <= ulp, (t, j)
+    # closed form: 16 equal chosen scores (identical logits, zero bias, one group) -> 5/32
+    E = 896
+    x = np.full((2, E), -4.0, np.float32)
+    x[:, 112:128] = 3.0
+    cfg = dict(logits=x, dtype="f32", bias=np.zeros(E, np.float32), T=2, E=E, k=16, G=8, Kg=4,
+               scale=2.5)
+    out = run(lib, cfg)
+    _, wb = unpack(out["packed"])
+    assert np.all(wb == 0x3E20)
+    assert np.array_equal(out["ids"][0], np.arange(112, 128))
+
+
+def pin_histogram_scan_perm(lib):
+    """counts = bincount, offsets = [0, cumsum], perm = stable argsort of the ids."""
+    for cfg in (gen.cfg0(), gen.cfg1(24), gen.cfg4(T=200, n_hot=50, off=336, cnt=112),
+                small_cfg(T=50, E=32, G=4, Kg=2, k=4, seed=94)):
+        out = run(lib, cfg)
+        lid, _ = unpack(out["packed"])
+        flat = lid.ravel()
+        NE = out["NE"]
+        assert np.array_equal(out["counts"], np.bincount(flat, minlength=NE))
+        assert np.array_equal(out["offsets"], np.concatenate([[0], np.cumsum(out["counts"])]))
+        assert np.array_equal(out["perm"], np.argsort(flat, kind="stable"))
+
+
+def check_invariants(out, cfg, kept_groups=None):
+    T, k, E, G = cfg["T"], cfg["k"], cfg["E"], cfg["G"]
+    off, cnt = cfg.get("off", 0), cfg.get("cnt", 0)
+    gsz = E // G
+    ids = out["ids"]
+    lid, wb = unpack(out["packed"])
+    for t in range(T):
+        assert len(set(ids[t].tolist())) == k
+        if kept_groups is not None:
+            assert set((ids[t] // gsz).tolist()) <= set(kept_groups[t].tolist())
+        assert len(set(lid[t].tolist())) == k
+    assert out["counts"].sum() == T * k
+    assert out["offsets"][-1] == T * k and np.all(np.diff(out["offsets"]) >= 0)
+    assert np.array_equal(np.sort(out["perm"]), np.arange(T * k))
+    w = gen.bf16_bits_to_f32(wb).astype(np.float64)
+    assert np.all(np.abs(w.sum(axis=1) - cfg["scale"]) <= 1e-2)
+    NE = out["NE"]
+    assert np.all(lid < NE)
+    if cnt > 0:
+        # num_experts: a multiple of 4 covering count + top_k, and nothing more
+        assert NE % 4 == 0 and cnt + k <= NE < cnt + k + 4
+        assert np.all(lid < cnt + k) and np.all(out["counts"][cnt + k:] == 0)
+        # round trip: local id -> global id
+        back = np.where(lid < cnt, lid + off,
+                        np.take_along_axis(ids, np.clip(lid - cnt, 0, k - 1), axis=1))
+        assert np.array_equal(back, ids)
+        # rank-local ids of other ranks' experts sit in the slot they occupy
+        other = lid >= cnt
+        assert np.array_equal((lid - cnt)[other], np.nonzero(other)[1])
+    else:
+        assert np.array_equal(lid, ids)
+
+
+def pin_invariants(lib):
+    for cfg in (gen.cfg0(), gen.cfg1(64), gen.cfg4(T=256, n_hot=64, cnt=112, off=448),
+                gen.cfg3(96, off=784, cnt=112), gen.cfg1(16, off=101, cnt=30),
+                gen.cfg1(9, off=0, cnt=113), small_cfg(T=40, E=32, G=4, Kg=2, k=4, seed=95)):
+        out = run(lib, cfg)
+        x = logits_f32(cfg)
+        _, kept = brute_force_rows(x, lib_sigmoid(lib, x), cfg["bias"], cfg["G"], cfg["Kg"],
+                                   cfg["k"])
+        check_invariants(out, cfg, kept)
+
+
+def pin_rank_local_matrix(lib):
+    """The page's test matrix: EP 2/8/16, first/middle/last rank, 1..64 tokens.  Local
+    ids are valid and round-trip, and the global outputs do not change."""
+    E, k = 896, 16
+    full = gen.cfg1(64, off=0, cnt=0)
+    g_out = run(lib, full)
+    for ep in (2, 8, 16):
+        cnt = E // ep
+        for rank in (0, ep // 2, ep - 1):
+            off = rank * cnt
+            for T in (1, 2, 7, 16, 33, 64):
+                cfg = gen.cfg1(T, off=off, cnt=cnt)
+                out = run(lib, cfg)
+                check_invariants(out, cfg)
+                assert np.array_equal(out["ids"], g_out["ids"][:T])
+                # entries of this rank's experts: same (token, slot, weight) in the same order
+                glid, gw = unpack(g_out["packed"][:T])
+                llid, lw = unpack(out["packed"])
+                assert np.array_equal(gw, lw)
+                gflat = glid.ravel()
+                gperm = np.argsort(gflat, kind="stable")
+                lperm = out["perm"]
+                for e in range(cnt):
+                    ge = gperm[gflat[gperm] == off + e]
+                    le = lperm[out["offsets"][e]:out["offsets"][e + 1]]
+                    assert np.array_equal(ge, le)
+
+
+def pin_page_facts(lib):
+    with open(os.path.join(GOLDEN, "page1_rank_local.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for E, k, ep, cnt, ne in ((int(v) for v in r) for r in rows):
+        assert E // ep == cnt
+        assert lib.oracle_num_experts(E, k, 3 * cnt, cnt) == ne
+    assert lib.oracle_num_experts(896, 16, 0, 0) == 896
+    with open(os.path.join(GOLDEN, "router_params.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    for E, H, L, billions in rows:
+        assert round(int(E) * int(H) * int(L) / 1e9, 2) == float(billions)
+
+
+def pin_router_gemm(lib):
+    """Double accumulation agrees with exact integer arithmetic on sampled outputs
+    (bf16 values are dyadic rationals) and with numpy's float64 matmul."""
+    T, H, E = 3, 256, 40
+    hid = gen.f32_to_bf16_bits(gen.normal_f32(501, T * H).reshape(T, H))
+    w = gen.f32_to_bf16_bits(gen.normal_f32(502, E * H, std=0.02).reshape(E, H))
+    out = oracle.router_gemm(hid, w, lib=lib)
+    hf = gen.bf16_bits_to_f32(hid).astype(np.float64)
+    wf = gen.bf16_bits_to_f32(w).astype(np.float64)
+    ref = hf @ wf.T
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+    for t, e in ((0, 0), (1, 17), (2, 39)):
+        exact = sum(Fraction(float(hf[t, h])) * Fraction(float(wf[e, h])) for h in range(H))
+        assert abs(Fraction(float(out[t, e])) - exact) <= abs(exact) * Fraction(1, 1 << 40) + \
+            Fraction(1, 1 << 60)
+
+
+def pin_rejects_invalid(lib):
+    cfg = gen.cfg0()
+    bad = [dict(G=5), dict(G=448, Kg=4, k=16), dict(Kg=0), dict(Kg=9), dict(k=113, Kg=1), dict(cnt=-1),
+           dict(off=800, cnt=112)]
+    for b in bad:
+        c = dict(cfg, **b)
+        try:
+            run(lib, c)
+        except ValueError:
+            continue
+        raise AssertionError(f"oracle accepted {b}")
+
+
+ALL_PINS = [
+    pin_sigmoid_exact, pin_sigmoid_symmetry, pin_bf16_rounding, pin_selection_brute_force,
+    pin_selection_exhaustive, pin_selection_kimi_shape, pin_plain_topk, pin_keep_all_groups_is_noop,
+    pin_weights, pin_histogram_scan_perm, pin_invariants, pin_rank_local_matrix, pin_page_facts,
+    pin_router_gemm, pin_rejects_invalid,
+]
