@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE routing hot path on GB300.
+
+Headline: prefill-scale routing, 65,536 token rows of the Kimi-K3 shape (896 experts,
+top_k 16, 8 groups of 112, keep 4, scale 2.5), bf16 logits N(0,1) plus Zipf(1.1)
+popularity offsets, float32 bias U(-0.1, 0.1), global ids.  One step = one moe_route
+call over the whole batch: scores, grouped top-k, weights, pack, histogram, scan and
+the stable permutation (one kernel launch).  value = routed tokens/s over all ranks.
+
+Also reported (same JSON line): decode routing latency at 8-64 rows (rank-local ids,
+CUDA-graph replay) against an empty-kernel floor replayed the same way, a roofline
+object for the prefill kernel, the CPU oracle's throughput on the machine's host, an
+end-to-end number with host buffers, and SM clocks sampled during the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torch.distributed.run; each rank routes its own batch (weak
+scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = "routing µs/call at 8–64 rows; routed tokens/s and HBM GB/s at 16K–64K rows"
+T_PREFILL = 65536
+E, K, G, KG, SCALE = 896, 16, 8, 4, 2.5
+# algorithmic bytes per routed row (global ids): bf16 logits in, packed + perm out
+BYTES_PER_ROW = E * 2 + K * 4 + K * 4
+NBUF = 4  # rotating input/output buffers: 4 x 117 MB of logits > 129 MB L2
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "route_prefill_bf16_T65536.json")
+
+
+def workload_cfg(T=T_PREFILL):
+    return dict(workload=f"prefill routing: T={T} rows, E={E}, top_k={K}, {G} groups of 112 keep "
+                         f"{KG}, scale {SCALE}, bf16 logits N(0,1)+0.5*ln(Zipf rank^-1.1) offsets, "
+                         f"fp32 bias U(-0.1,0.1), global ids; histogram, exclusive scan, stable "
+                         f"(expert, token, slot) permutation",
+                T=T, E=E, top_k=K, n_group=G, topk_group=KG,
+                l2=f"{NBUF} rotating input/output buffer sets ({NBUF * T * E * 2 / 1e6:.0f} MB of "
+                   f"logits, larger than the 129 MB L2)")
+
+
+def algorithmic_bytes(T, NE=E):
+    return T * BYTES_PER_ROW + NE * 4 + (NE + 1) * 4 + E * 4
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "serving_moe_route_02_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", self.gpu_id, "-lms", "50"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == 0:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or 1e30)]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(p[1]) for _, p in use if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, p in use for i in range(4) if p[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(use), "sampled_during": "timed region" if inside else "bench run"}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_baseline(min_seconds=10.0, max_reps=5):
+    """The oracle as it stands, single-threaded, on the full 65,536-row workload."""
+    import oracle
+    cfg = gen.cfg3(T_PREFILL)
+    times = []
+    t_all = time.time()
+    while len(times) < max_reps and (time.time() - t_all < min_seconds or len(times) < 1):
+        t = time.perf_counter()
+        oracle.route_cfg(cfg)
+        times.append(time.perf_counter() - t)
+    med = statistics.median(times)
+    return {"value": T_PREFILL / med, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"full {T_PREFILL}-row call of the same workload, median of {len(times)} "
+                      f"single-threaded runs ({med:.2f} s each)",
+            "cpu": _cpu_name(), "nproc": os.cpu_count()}
+
+
+def _cpu_name():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    cfg = gen.cfg3(T_PREFILL)
+    # bounded sample per step: the whole run stays within about a minute of CPU time
+    rows = int(max(16, min(T_PREFILL, 60.0 * 15000.0 / max(1, args.steps + args.warmup))))
+    def step(i):
+        lo = (i * rows) % (T_PREFILL - rows + 1)
+        sub = dict(cfg, logits=cfg["logits"][lo:lo + rows], T=rows)
+        oracle.route_cfg(sub)
+    for i in range(args.warmup):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t
+    value = rows * args.steps / dt
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference", "config": workload_cfg(),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} rows of the {T_PREFILL}-row workload per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def to_dev_bf16(torch, arr, dev):
+    return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def decode_latency(torch, mr, dev, reps=200, replays=10):
+    """µs per call under CUDA-graph replay (rank-local ids, offset 336, count 112),
+    against an empty kernel with the same launch shape replayed the same way."""
+    res = {"T": [], "us_per_call": [], "floor_us": [], "ratio_to_floor": []}
+    st = torch.cuda.Stream(device=dev)
+    for T in (8, 16, 24, 32, 64):
+        cfg = gen.cfg1(T)
+        lg = to_dev_bf16(torch, cfg["logits"], dev)
+        bias = torch.from_numpy(cfg["bias"]).to(dev)
+        out = mr.alloc_outputs(T, E, K, 112, dev)
+        ctas = (T + 7) // 8
+        with torch.cuda.stream(st):
+            mr.route(lg, bias, local_offset=336, local_count=112, out=out, stream=st)
+            mr.empty_kernel(ctas, stream=st)
+            st.synchronize()
+            g_route = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_route, stream=st):
+                for _ in range(reps):
+                    mr.route(lg, bias, local_offset=336, local_count=112, out=out, stream=st)
+            g_empty = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_empty, stream=st):
+                for _ in range(reps):
+                    mr.empty_kernel(ctas, stream=st)
+        times = {}
+        for name, g in (("route", g_route), ("empty", g_empty)):
+            g.replay()
+            torch.cuda.synchronize()
+            samples = []
+            for _ in range(replays):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                g.replay()
+                b.record(st)
+                b.synchronize()
+                samples.append(a.elapsed_time(b) * 1e3 / reps)
+            times[name] = statistics.median(samples)
+        res["T"].append(T)
+        res["us_per_call"].append(round(times["route"], 3))
+        res["floor_us"].append(round(times["empty"], 3))
+        res["ratio_to_floor"].append(round(times["route"] / times["empty"], 3))
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import torch.distributed as dist
+    import serving_moe_route_02_gb300 as mr
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    mr.load()
+    mr.reserve()
+
+    cfg = gen.cfg3(T_PREFILL)
+    host_logits = np.ascontiguousarray(cfg["logits"])
+    bufs = [to_dev_bf16(torch, host_logits, dev) for _ in range(NBUF)]
+    bias = torch.from_numpy(cfg["bias"]).to(dev)
+    outs = [mr.alloc_outputs(T_PREFILL, E, K, 0, dev) for _ in range(NBUF)]
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        mr.route(bufs[i % NBUF], bias, out=outs[i % NBUF])
+    torch.cuda.synchronize()
+    if mr.device_status() != 0:
+        raise SystemExit("device status error during warm-up")
+
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark(0)
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        mr.route(bufs[i % NBUF], bias, out=outs[i % NBUF])
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark(1)
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    kernel_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if world > 1:
+        tt = torch.tensor([elapsed_ms, kernel_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms, kernel_ms = float(tt[0]), float(tt[1])
+    status = mr.device_status()
+    # The timed region may be too short for 50 ms clock samples; then sample a 1 s run of
+    # the same kernel right after it and say so.
+    n_inside = sum(1 for ts, _ in sampler.lines if sampler.t0 <= ts <= sampler.t1)
+    probe = n_inside < 3
+    if probe:
+        sampler.mark(0)
+        t_probe = time.time()
+        while time.time() - t_probe < 1.0:
+            for i in range(200):
+                mr.route(bufs[i % NBUF], bias, out=outs[i % NBUF])
+            torch.cuda.synchronize()
+        sampler.mark(1)
+    sampler.stop()
+    clocks = sampler.summary()
+    if probe and clocks.get("sampled_during") == "timed region":
+        clocks["sampled_during"] = "1 s run of the same kernel right after the timed region"
+
+    # sanity check of the last output against invariants (torch ops, outside timing)
+    o = outs[(args.steps - 1) % NBUF]
+    ok = bool(int(o["counts"].sum()) == T_PREFILL * K and int(o["offsets"][-1]) == T_PREFILL * K
+              and torch.equal(torch.sort(o["perm"].long()).values,
+                              torch.arange(T_PREFILL * K, device=dev)))
+
+    # end to end: pinned host logits -> device -> route -> outputs back to pinned host
+    h_in = torch.from_numpy(host_logits.view(np.int16)).pin_memory()
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()
+             if v is not None}
+    d_in = bufs[0]
+    e2e_steps = max(3, min(args.steps, 100))
+    h2d = h_in.numel() * 2
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    for _ in range(2):
+        d_in.view(torch.int16).copy_(h_in, non_blocking=True)
+        mr.route(d_in, bias, out=outs[0])
+        for k2, v in h_out.items():
+            v.copy_(outs[0][k2], non_blocking=True)
+    torch.cuda.synchronize()
+    ea = torch.cuda.Event(enable_timing=True)
+    eb = torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        d_in.view(torch.int16).copy_(h_in, non_blocking=True)
+        mr.route(d_in, bias, out=outs[0])
+        for k2, v in h_out.items():
+            v.copy_(outs[0][k2], non_blocking=True)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt[0])
+
+    decode = None
+    if rank == 0 and not args.no_decode:
+        decode = decode_latency(torch, mr, dev)
+
+    peaks, peak_src = measured_peaks()
+    ab = algorithmic_bytes(T_PREFILL)
+    achieved = ab / (kernel_ms * 1e-3) / 1e9
+    traffic = None
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            prof = json.load(f)
+        if prof.get("csrc_hash") == csrc_hash():
+            traffic = prof.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    ms_per_step = elapsed_ms / args.steps
+    value = world * T_PREFILL / (ms_per_step * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_cfg(),
+        "hbm_gbs": ab / (ms_per_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "k_route_prefill<bf16>", "algorithmic_bytes": ab,
+                     "kernel_us": kernel_ms * 1e3, "peak_source": f"{peak_src} hbm_gbs (copy)"},
+        "clocks": clocks,
+        "e2e": {"value": world * T_PREFILL / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "device_status": status, "invariants_ok": ok,
+    }
+    if decode is not None:
+        line["decode"] = decode
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

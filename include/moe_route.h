@@ -1,0 +1,157 @@
+/*
+ * moe_route.h -- C ABI of the GB300 (sm_103a) MoE token-to-expert routing library.
+ *
+ * One routing call, per token row t of a [T, E] logit matrix:
+ *   s_e = sigmoid(logit_e); b_e = s_e + bias_e            (a1, a2)
+ *     "a sigmoid router with correction bias and grouped top-k"
+ *     -- vLLM PR #59693 (ROCm token-sharded residual), description of its KimiMoE test.
+ *   group score = sum of the two largest b of each group of E/n_group consecutive
+ *   experts; keep the topk_group groups with the largest score (ties: lower group);
+ *   choose the k largest b among the kept experts (ties: lower expert id); slot j
+ *   of the row is the j-th of them in (b descending, id ascending) order   (a3-a5)
+ *   w_j = bf16_rne(float(float(s_j / sum_slots s) * scale))                (a6)
+ *   optional rank-local relabel: experts in [local_offset, local_offset +
+ *   local_count) become 0..local_count-1, any other expert in slot j becomes
+ *   local_count + j; num_experts NE = round_up(local_count + k, 4)         (a7)
+ *   packed[t][j] = (id << 16) | bits(w_j)                                  (a8)
+ *     -- sglang PR #37 "Rank-local expert ids for the EP routed MoE", description
+ *        ("packed (id << 16 | bf16 weight) ids"; "the rank's experts as 0..count-1
+ *        and any other expert in top-k slot k as count + k (unique per row)";
+ *        "num_experts = round_up(count + top_k, 4)").
+ * and over all rows:
+ *   counts[e]  = number of entries with (relabelled) id e, e in [0, NE)     (a9)
+ *   offsets    = exclusive scan of counts, offsets[NE] = T * k              (a10)
+ *   perm[offsets[e] + r] = t * k + j for the r-th entry of id e in (t, j) order (a11)
+ *     -- same passage: "the same (token, local expert, weight) entries reach the
+ *        expert GEMMs in the same order".
+ * The Kimi-K3 instance is E = 896, k = 16, n_group = 8 (112 experts each),
+ * topk_group = 4, scale = 2.5 (sglang PR #37: "Tier<896, 16>", "112 of 896 at EP8").
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; the library never
+ *     frees them.  Arrays are dense and row-major.  logits must be 16-byte aligned.
+ *   - Work is enqueued on `stream` without host synchronisation, so calls can be
+ *     captured in a CUDA graph once the library's per-device state exists (call
+ *     moe_route_reserve() before capture).  Outputs are fully overwritten; no
+ *     zeroing is needed.
+ *   - Calls on one device share one workspace: calls must be ordered on the GPU
+ *     (same stream, or otherwise serialised); concurrent calls race.
+ *   - Return value: MOE_ROUTE_OK or a negative moe_route_status.  A call that returns
+ *     an error has enqueued nothing.  Errors detected on the device (a bounded wait
+ *     that ran out) are reported by moe_route_device_status().
+ *   - Supported shapes: E = 896 with n_group = 8 (the Kimi-K3 grouping), any
+ *     topk_group in [1, 8], 1 <= k <= 32 with k <= topk_group * 112.  Other valid
+ *     shapes return MOE_ROUTE_E_UNSUPPORTED.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st*`; NULL = legacy default stream */
+
+typedef enum {
+    MOE_ROUTE_OK = 0,
+    MOE_ROUTE_E_INVALID_ARG = -1,    /* arguments violate the definition or a pointer is NULL */
+    MOE_ROUTE_E_UNSUPPORTED = -2,    /* valid, but not a shape the kernels implement */
+    MOE_ROUTE_E_CUDA = -3,           /* a CUDA runtime call failed (launch, allocation) */
+    MOE_ROUTE_E_WORKSPACE = -4,      /* per-device state missing while the stream is capturing */
+    MOE_ROUTE_E_DEVICE_TIMEOUT = -5  /* a bounded device-side wait ran out (see device_status) */
+} moe_route_status;
+
+typedef enum { MOE_ROUTE_F32 = 0, MOE_ROUTE_BF16 = 1 } moe_route_dtype;
+
+/*
+ * moe_route -- steps a1..a11 for a [T, E] matrix of router logits.
+ *   logits        [T, E] float32 (dtype MOE_ROUTE_F32) or bfloat16 bits (MOE_ROUTE_BF16),
+ *                 16-byte aligned.  Must be finite.
+ *   bias          [E] float32 correction bias (selection only; weights use s).
+ *   T >= 0; T = 0 writes zero counts and offsets only.
+ *   E, k, n_group, topk_group, scale   as defined above; scale is routed_scaling_factor.
+ *   local_offset, local_count  rank-local relabel range; local_count = 0 keeps global ids.
+ *                 0 <= local_offset, local_offset + local_count <= E.
+ *   packed        [T, k] int32 out: (id << 16) | bf16 weight bits (id relabelled if asked).
+ *   counts        [NE] int32 out, offsets [NE + 1] int32 out, perm [T * k] int32 out,
+ *                 NE = moe_route_bins(E, k, local_count).
+ *   topk_ids      [T, k] int32 out, nullable: the GLOBAL expert ids in slot order.
+ * Errors: INVALID_ARG when E % n_group != 0, E / n_group < 2, topk_group not in
+ * [1, n_group], k < 1 or k > topk_group * E / n_group, T < 0, a required pointer is
+ * NULL, logits not 16-byte aligned, local_count < 0, local_offset < 0,
+ * local_offset + local_count > E, or an id would not fit 15 bits.
+ */
+int moe_route(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+              int n_group, int topk_group, float scale, int local_offset, int local_count,
+              int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
+              int32_t* topk_ids, struct CUstream_st* stream);
+
+/*
+ * moe_router_gemm_route -- router contraction a0 fused in front of moe_route:
+ *   logits[t][e] = sum_h hidden[t][h] * w_router[e][h], bf16 inputs, fp32 accumulate,
+ * then steps a1..a11 on those fp32 logits.  The router weight is 896 x 7168 per layer
+ * (HartsyInference PR #798, "Memory per GPU": router 0.59 B parameters over 92 layers).
+ *   hidden      [T, H] bf16 bits, 16-byte aligned; w_router [E, H] bf16 bits (row e =
+ *               expert e), 16-byte aligned.  H % 64 == 0.
+ *   1 <= T <= 64 (decode batches).
+ *   logits_out  [T, E] float32 out, nullable (the fp32 logits the routing used).
+ *   other arguments as moe_route.  Supported: E = 896, n_group = 8, H % 64 == 0.
+ */
+int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, const float* bias,
+                          int T, int H, int E, int k, int n_group, int topk_group, float scale,
+                          int local_offset, int local_count, float* logits_out, int32_t* packed,
+                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* topk_ids,
+                          struct CUstream_st* stream);
+
+/* Number of expert bins the outputs use: local_count > 0 ? round_up(local_count + k, 4) : E. */
+int moe_route_bins(int E, int k, int local_count);
+
+/*
+ * Policy helper (sglang PR #37: rank-local ids apply only to "a proper sub-range that
+ * shrinks the routing problem"): returns round_up(local_count + k, 4) when
+ * 0 < local_count < E and that is smaller than E; otherwise E, meaning the caller
+ * should pass local_count = 0 (global ids).
+ */
+int moe_route_num_experts(int E, int k, int local_offset, int local_count);
+
+/*
+ * Creates the current device's library state (workspace, sigmoid table for bf16
+ * logits, kernel attributes).  Call once per device before capturing calls in a CUDA
+ * graph; calls outside capture create it on first use.  Allocates with cudaMalloc.
+ */
+int moe_route_reserve(void);
+
+/*
+ * Waits for the current device, returns and clears the device-side error word
+ * (MOE_ROUTE_OK or MOE_ROUTE_E_DEVICE_TIMEOUT), and resets the workspace's barrier
+ * state after an error.
+ */
+int moe_route_device_status(void);
+
+/* Elementwise step a1 as the routing kernels compute it: s[i] = sigmoid(x[i]).
+ * x: [n] float32 or bf16 bits (device), s: [n] float32 (device). */
+int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream_st* stream);
+
+/*
+ * Kernel selection for moe_route: 0 = automatic (T <= 64: one-cluster decode kernel,
+ * otherwise the persistent multi-CTA kernel), 1 = always the decode kernel (T <= 64
+ * only), 2 = always the persistent kernel.  Process-wide; for tests and benchmarks.
+ * Returns the previous setting, or MOE_ROUTE_E_INVALID_ARG.
+ */
+int moe_route_set_path(int path);
+
+/*
+ * Measurement helper: enqueues one launch of an empty kernel with the decode kernel's
+ * launch shape (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 8).  Replayed in a
+ * CUDA graph it gives the launch-latency floor that decode routing is compared with.
+ */
+int moe_route_empty(int ctas, struct CUstream_st* stream);
+
+/* Static description of a status code. */
+const char* moe_route_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -50,6 +50,8 @@ def _bind(lib):
     I = ctypes.c_int
     lib.oracle_sigmoid.argtypes = [ctypes.c_float]
     lib.oracle_sigmoid.restype = ctypes.c_float
+    lib.oracle_sigmoid_array.argtypes = [P, I, P, ctypes.c_long]
+    lib.oracle_sigmoid_array.restype = None
     lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
     lib.oracle_num_experts.argtypes = [I, I, I, I]
@@ -69,10 +71,13 @@ def num_experts(E: int, k: int, off: int, cnt: int, lib=None) -> int:
     return (lib or load()).oracle_num_experts(E, k, off, cnt)
 
 
-def sigmoid(x: np.ndarray, lib=None) -> np.ndarray:
+def sigmoid(x: np.ndarray, dtype: str = "f32", lib=None) -> np.ndarray:
+    """Oracle scores of an array of float32 values or bf16 bit patterns (same shape)."""
     lib = lib or load()
-    x = np.asarray(x, dtype=np.float32).ravel()
-    return np.array([lib.oracle_sigmoid(float(v)) for v in x], dtype=np.float32)
+    xa = np.ascontiguousarray(x, dtype=np.float32 if dtype == "f32" else np.uint16)
+    s = np.empty(xa.shape, dtype=np.float32)
+    lib.oracle_sigmoid_array(_ptr(xa), DT[dtype], _ptr(s), xa.size)
+    return s
 
 
 def f32_to_bf16(x: np.ndarray, lib=None) -> np.ndarray:

@@ -46,6 +46,14 @@ float oracle_sigmoid(float x) {
     return (float)s;
 }
 
+void oracle_sigmoid_array(const void* x, int dtype, float* s, long n) {
+    for (long i = 0; i < n; ++i) {
+        float v = (dtype == ORACLE_DT_F32) ? ((const float*)x)[i]
+                                           : f32_from_bf16(((const uint16_t*)x)[i]);
+        s[i] = oracle_sigmoid(v);
+    }
+}
+
 int oracle_num_experts(int E, int k, int local_offset, int local_count) {
     (void)local_offset;
     if (local_count <= 0) return E;

@@ -47,6 +47,9 @@ enum { ORACLE_DT_F32 = 0, ORACLE_DT_BF16 = 1 };
 /* sigma(x) = 1 / (1 + e^-x) evaluated in double, rounded once to float. */
 float oracle_sigmoid(float x);
 
+/* s[i] = oracle_sigmoid(x[i]) for i < n; x is float (dtype 0) or bf16 bits (dtype 1). */
+void oracle_sigmoid_array(const void* x, int dtype, float* s, long n);
+
 /* float -> bfloat16 bits, round to nearest, ties to even (finite inputs). */
 uint16_t oracle_f32_to_bf16(float x);
 

@@ -1,0 +1,184 @@
+"""Python binding of the GB300 MoE routing library (libmoe_route.so).
+
+Argument marshalling only: every step of the routing path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors; the binding passes their data
+pointers and the current CUDA stream to the C ABI declared in include/moe_route.h.
+There is no CPU fallback: if the shared library is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_route.so")
+
+OK = 0
+E_INVALID_ARG = -1
+E_UNSUPPORTED = -2
+E_CUDA = -3
+E_WORKSPACE = -4
+E_DEVICE_TIMEOUT = -5
+F32 = 0
+BF16 = 1
+
+_lib = None
+
+
+class MoeRouteError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} ({status})")
+
+
+def load(path: str | None = None):
+    """Load libmoe_route.so (built by __graft_entry__.build() or _build.build())."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise ImportError(f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                          f"g.build()')")
+    lib = ctypes.CDLL(p)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.moe_route.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P]
+    lib.moe_route.restype = I
+    lib.moe_router_gemm_route.argtypes = [P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
+    lib.moe_router_gemm_route.restype = I
+    lib.moe_route_bins.argtypes = [I, I, I]
+    lib.moe_route_bins.restype = I
+    lib.moe_route_num_experts.argtypes = [I, I, I, I]
+    lib.moe_route_num_experts.restype = I
+    lib.moe_route_reserve.argtypes = []
+    lib.moe_route_reserve.restype = I
+    lib.moe_route_device_status.argtypes = []
+    lib.moe_route_device_status.restype = I
+    lib.moe_route_sigmoid.argtypes = [P, I, P, I, P]
+    lib.moe_route_sigmoid.restype = I
+    lib.moe_route_set_path.argtypes = [I]
+    lib.moe_route_set_path.restype = I
+    lib.moe_route_empty.argtypes = [I, P]
+    lib.moe_route_empty.restype = I
+    lib.moe_route_strerror.argtypes = [I]
+    lib.moe_route_strerror.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load().moe_route_strerror(status).decode()
+    except ImportError:
+        return f"status {status}"
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise MoeRouteError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def bins(E: int, k: int, local_count: int) -> int:
+    return load().moe_route_bins(E, k, local_count)
+
+
+def num_experts(E: int, k: int, local_offset: int, local_count: int) -> int:
+    return load().moe_route_num_experts(E, k, local_offset, local_count)
+
+
+def reserve():
+    _check(load().moe_route_reserve(), "moe_route_reserve")
+
+
+def device_status() -> int:
+    return load().moe_route_device_status()
+
+
+def set_path(path: int) -> int:
+    rc = load().moe_route_set_path(path)
+    if rc < 0:
+        raise MoeRouteError(rc, "moe_route_set_path")
+    return rc
+
+
+def alloc_outputs(T: int, E: int, k: int, local_count: int, device, want_ids: bool = False) -> dict:
+    NE = bins(E, k, local_count)
+    out = dict(packed=torch.empty((T, k), dtype=torch.int32, device=device),
+               counts=torch.empty(NE, dtype=torch.int32, device=device),
+               offsets=torch.empty(NE + 1, dtype=torch.int32, device=device),
+               perm=torch.empty(T * k, dtype=torch.int32, device=device))
+    out["ids"] = torch.empty((T, k), dtype=torch.int32, device=device) if want_ids else None
+    return out
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype in (torch.bfloat16, torch.int16, torch.uint16):
+        return BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int = 8,
+          topk_group: int = 4, scale: float = 2.5, local_offset: int = 0, local_count: int = 0,
+          out: dict | None = None, want_ids: bool = False, stream=None) -> dict:
+    """moe_route on a [T, E] CUDA tensor of router logits (float32 or bfloat16)."""
+    if not (logits.is_cuda and bias.is_cuda):
+        raise ValueError("logits and bias must be CUDA tensors")
+    if not logits.is_contiguous() or not bias.is_contiguous() or bias.dtype != torch.float32:
+        raise ValueError("logits and bias must be contiguous; bias float32")
+    T, E = logits.shape
+    if out is None:
+        out = alloc_outputs(T, E, k, local_count, logits.device, want_ids)
+    rc = load().moe_route(_ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group,
+                          topk_group, float(scale), local_offset, local_count, _ptr(out["packed"]),
+                          _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]),
+                          _ptr(out.get("ids")), _stream(stream))
+    _check(rc, "moe_route")
+    return out
+
+
+def router_gemm_route(hidden: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor, *,
+                      k: int = 16, n_group: int = 8, topk_group: int = 4, scale: float = 2.5,
+                      local_offset: int = 0, local_count: int = 0, want_logits: bool = True,
+                      out: dict | None = None, want_ids: bool = False, stream=None) -> dict:
+    """moe_router_gemm_route: bf16 hidden [T, H] x router weight [E, H] -> routing."""
+    T, H = hidden.shape
+    E = w_router.shape[0]
+    if out is None:
+        out = alloc_outputs(T, E, k, local_count, hidden.device, want_ids)
+    if want_logits and out.get("logits") is None:
+        out["logits"] = torch.empty((T, E), dtype=torch.float32, device=hidden.device)
+    rc = load().moe_router_gemm_route(_ptr(hidden), _ptr(w_router), _ptr(bias), T, H, E, k, n_group,
+                                      topk_group, float(scale), local_offset, local_count,
+                                      _ptr(out.get("logits")), _ptr(out["packed"]),
+                                      _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]),
+                                      _ptr(out.get("ids")), _stream(stream))
+    _check(rc, "moe_router_gemm_route")
+    return out
+
+
+def empty_kernel(ctas: int = 1, stream=None):
+    """Launch the empty floor kernel (decode launch shape)."""
+    _check(load().moe_route_empty(ctas, _stream(stream)), "moe_route_empty")
+
+
+def sigmoid(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """Step a1 exactly as the routing kernels compute it."""
+    s = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    rc = load().moe_route_sigmoid(_ptr(x), _dtype_code(x), _ptr(s), x.numel(), _stream(stream))
+    _check(rc, "moe_route_sigmoid")
+    return s

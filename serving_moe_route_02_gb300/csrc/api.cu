@@ -1,0 +1,240 @@
+// api.cu -- the C ABI (include/moe_route.h): argument checks, per-device state and
+// dispatch to the routing kernels.  No routing arithmetic happens on the host.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_route.h"
+#include "launch.h"
+
+namespace {
+
+using namespace moe;
+
+struct DevState {
+  bool ready = false;
+  int nsm = 0;
+  int blocks_per_sm = 0;
+  float* stab = nullptr;  // sigmoid table for bf16 logits
+  int* err = nullptr;     // device status word
+  PrefillWS pw = {};
+  int* pw_block = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DevState g_dev[kMaxDevices];
+std::mutex g_mu;
+int g_path = 0;
+
+bool capturing(cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return false;
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+// Creates the current device's state.  Must not run during stream capture.
+int init_device(DevState& d) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ROUTE_E_CUDA;
+  if (setup_decode_kernels() != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (setup_prefill_kernels(&d.blocks_per_sm) != cudaSuccess || d.blocks_per_sm < 1)
+    return MOE_ROUTE_E_CUDA;
+  const int grid_max = d.nsm * d.blocks_per_sm;
+  const size_t n_tab = size_t(kSigTablePad);
+  const size_t n_hist = size_t(kMaxBins) * grid_max;
+  // one block: [table][hist][prefix][counts][bar x2, err, pad]
+  const size_t bytes = n_tab * 4 + 2 * n_hist * 4 + size_t(kMaxBins) * 4 + 64;
+  int* blk = nullptr;
+  if (cudaMalloc(&blk, bytes) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (cudaMemset(blk, 0, bytes) != cudaSuccess) {
+    cudaFree(blk);
+    return MOE_ROUTE_E_CUDA;
+  }
+  d.pw_block = blk;
+  d.stab = reinterpret_cast<float*>(blk);
+  d.pw.hist = blk + n_tab;
+  d.pw.prefix = d.pw.hist + n_hist;
+  d.pw.counts = d.pw.prefix + n_hist;
+  d.pw.bar = reinterpret_cast<unsigned*>(d.pw.counts + kMaxBins);
+  d.err = reinterpret_cast<int*>(d.pw.bar + 2);
+  d.pw.grid_max = grid_max;
+  if (launch_sigmoid_table(d.stab, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  d.ready = true;
+  return MOE_ROUTE_OK;
+}
+
+// Returns the current device's state, creating it outside capture.
+int get_state(cudaStream_t st, DevState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ROUTE_E_CUDA;
+  DevState& d = g_dev[dev];
+  if (!d.ready) {
+    if (st != nullptr && capturing(st)) return MOE_ROUTE_E_WORKSPACE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!d.ready) {
+      const int rc = init_device(d);
+      if (rc != MOE_ROUTE_OK) return rc;
+    }
+  }
+  *out = &d;
+  return MOE_ROUTE_OK;
+}
+
+int bins(int E, int k, int cnt) { return cnt > 0 ? (cnt + k + 3) / 4 * 4 : E; }
+
+int check_route_args(int T, int E, int k, int n_group, int topk_group, int off, int cnt) {
+  if (T < 0 || E <= 0 || k <= 0 || n_group <= 0) return MOE_ROUTE_E_INVALID_ARG;
+  if (E % n_group != 0 || E / n_group < 2) return MOE_ROUTE_E_INVALID_ARG;
+  if (topk_group < 1 || topk_group > n_group) return MOE_ROUTE_E_INVALID_ARG;
+  if (k > topk_group * (E / n_group)) return MOE_ROUTE_E_INVALID_ARG;
+  if (cnt < 0 || off < 0 || off + cnt > E) return MOE_ROUTE_E_INVALID_ARG;
+  if (E > 32767 || (cnt > 0 && cnt + k > 32767)) return MOE_ROUTE_E_INVALID_ARG;
+  if (static_cast<long long>(T) * k >= (1ll << 31)) return MOE_ROUTE_E_INVALID_ARG;
+  if (E != kE || n_group != kG || k > kMaxK) return MOE_ROUTE_E_UNSUPPORTED;
+  if (bins(E, k, cnt) > kMaxBins) return MOE_ROUTE_E_UNSUPPORTED;
+  return MOE_ROUTE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_route_bins(int E, int k, int local_count) { return bins(E, k, local_count); }
+
+int moe_route_num_experts(int E, int k, int local_offset, int local_count) {
+  (void)local_offset;
+  if (local_count <= 0 || local_count >= E) return E;
+  const int ne = bins(E, k, local_count);
+  return ne < E ? ne : E;
+}
+
+int moe_route_reserve(void) {
+  DevState* d = nullptr;
+  return get_state(nullptr, &d);
+}
+
+int moe_route(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+              int n_group, int topk_group, float scale, int local_offset, int local_count,
+              int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
+              int32_t* topk_ids, struct CUstream_st* stream) {
+  int rc = check_route_args(T, E, k, n_group, topk_group, local_offset, local_count);
+  if (rc != MOE_ROUTE_OK) return rc;
+  if (logits_dtype != MOE_ROUTE_F32 && logits_dtype != MOE_ROUTE_BF16) return MOE_ROUTE_E_INVALID_ARG;
+  if (!bias || !counts || !offsets) return MOE_ROUTE_E_INVALID_ARG;
+  if (T > 0 && (!logits || !packed || !perm)) return MOE_ROUTE_E_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % 16 != 0 || reinterpret_cast<uintptr_t>(bias) % 16 != 0)
+    return MOE_ROUTE_E_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevState* d = nullptr;
+  rc = get_state(st, &d);
+  if (rc != MOE_ROUTE_OK) return rc;
+
+  RouteArgs a = {};
+  a.logits = logits;
+  a.bias = bias;
+  a.stab = d->stab;
+  a.packed = packed;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.ids = topk_ids;
+  a.err = d->err;
+  a.T = T;
+  a.k = k;
+  a.Kg = topk_group;
+  a.off = local_offset;
+  a.cnt = local_count;
+  a.NE = bins(E, k, local_count);
+  a.scale = scale;
+  const int dt = logits_dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32;
+
+  const bool decode = (g_path == 1) || (g_path == 0 && T <= 64);
+  cudaError_t ce;
+  if (decode) {
+    if (T > 64) return MOE_ROUTE_E_UNSUPPORTED;
+    ce = launch_route_decode(a, dt, st);
+  } else {
+    if (T == 0) {
+      ce = launch_route_decode(a, dt, st);
+    } else {
+      const int grid_cap = d->pw.grid_max;
+      int grid = (T + 15) / 16;
+      if (grid > grid_cap) grid = grid_cap;
+      ce = launch_route_prefill(a, dt, d->pw, grid, st);
+    }
+  }
+  return ce == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
+}
+
+int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, const float* bias,
+                          int T, int H, int E, int k, int n_group, int topk_group, float scale,
+                          int local_offset, int local_count, float* logits_out, int32_t* packed,
+                          int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* topk_ids,
+                          struct CUstream_st* stream) {
+  (void)hidden; (void)w_router; (void)bias; (void)T; (void)H; (void)E; (void)k; (void)n_group;
+  (void)topk_group; (void)scale; (void)local_offset; (void)local_count; (void)logits_out;
+  (void)packed; (void)counts; (void)offsets; (void)perm; (void)topk_ids; (void)stream;
+  return MOE_ROUTE_E_UNSUPPORTED;
+}
+
+int moe_route_device_status(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ROUTE_E_CUDA;
+  DevState& d = g_dev[dev];
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (!d.ready) return MOE_ROUTE_OK;
+  int host = 0;
+  if (cudaMemcpy(&host, d.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ROUTE_E_CUDA;
+  if (host != 0) {
+    // clear the status word and the grid barrier state left by the failed call
+    if (cudaMemset(d.err, 0, sizeof(int)) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+    if (cudaMemset(d.pw.bar, 0, 2 * sizeof(unsigned)) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  }
+  return host;
+}
+
+int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream_st* stream) {
+  if (n < 0 || (n > 0 && (!x || !s))) return MOE_ROUTE_E_INVALID_ARG;
+  if (dtype != MOE_ROUTE_F32 && dtype != MOE_ROUTE_BF16) return MOE_ROUTE_E_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevState* d = nullptr;
+  const int rc = get_state(st, &d);
+  if (rc != MOE_ROUTE_OK) return rc;
+  return launch_sigmoid(x, dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32, d->stab, s, n, st) ==
+                 cudaSuccess
+             ? MOE_ROUTE_OK
+             : MOE_ROUTE_E_CUDA;
+}
+
+int moe_route_set_path(int path) {
+  if (path < 0 || path > 2) return MOE_ROUTE_E_INVALID_ARG;
+  const int prev = g_path;
+  g_path = path;
+  return prev;
+}
+
+int moe_route_empty(int ctas, struct CUstream_st* stream) {
+  if (ctas < 1 || ctas > 8) return MOE_ROUTE_E_INVALID_ARG;
+  return launch_empty(ctas, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_ROUTE_OK
+                                                                                     : MOE_ROUTE_E_CUDA;
+}
+
+const char* moe_route_strerror(int status) {
+  switch (status) {
+    case MOE_ROUTE_OK: return "ok";
+    case MOE_ROUTE_E_INVALID_ARG: return "invalid argument";
+    case MOE_ROUTE_E_UNSUPPORTED: return "shape not supported by the kernels";
+    case MOE_ROUTE_E_CUDA: return "CUDA runtime error";
+    case MOE_ROUTE_E_WORKSPACE: return "library state missing during stream capture";
+    case MOE_ROUTE_E_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

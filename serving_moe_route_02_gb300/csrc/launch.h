@@ -1,0 +1,31 @@
+// launch.h -- host-side launchers of the routing kernels (internal to the library).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "route_row.cuh"
+
+namespace moe {
+
+// Per-device workspace of the persistent kernel (device memory, zeroed at creation).
+struct PrefillWS {
+  int* hist;       // [kMaxBins][grid_max] per-CTA histograms, expert-major
+  int* prefix;     // [kMaxBins][grid_max] exclusive prefix over CTAs
+  int* counts;     // [kMaxBins]
+  unsigned* bar;   // [2]: arrival count, generation
+  int grid_max;
+};
+
+constexpr int kSigTablePad = (kSigTable + 3) / 4 * 4;  // table length rounded to 16 bytes
+
+cudaError_t launch_sigmoid_table(float* tab, cudaStream_t st);
+cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, float* s, int n,
+                           cudaStream_t st);
+cudaError_t setup_decode_kernels();
+cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st);
+cudaError_t launch_empty(int ctas, cudaStream_t st);
+cudaError_t setup_prefill_kernels(int* blocks_per_sm);
+cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,
+                                 cudaStream_t st);
+
+}  // namespace moe

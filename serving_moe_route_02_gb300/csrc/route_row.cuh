@@ -1,0 +1,316 @@
+// route_row.cuh -- one warp routes one token row of 896 router logits.
+//
+// Steps per row (the method, as defined in moe_route.h):
+//   s = sigmoid(x), b = s + bias                    lane l owns experts [28 l, 28 l + 28)
+//   group score = top-2 sum of b over 112 experts   lane top-2, then a 4-lane merge
+//   keep topk_group groups                          rank of each group among the 8 scores
+//   top-k of b over kept experts, ties to lower id  threshold + compaction + warp argmax
+//   weights, relabel, pack                          lanes 0..k-1 hold slots 0..k-1
+//
+// Selection.  tau0 = the k-th largest value of a pool made of the two largest b of
+// every kept lane (a subset of the candidates, so at least k candidates reach tau0).
+// Candidates with b >= tau0 ("survivors", typically 17-22 for k = 16) are compacted
+// one per lane in expert-id order; k rounds of a warp max then pick the slots, the
+// lowest lane (= lowest id) winning exact ties.  If more than 32 survive, a slower
+// exact path extracts the k winners from per-lane maxima.
+#pragma once
+#include "common.cuh"
+
+namespace moe {
+
+struct RouteArgs {
+  const void* logits;     // [T, E] f32 or bf16 bits
+  const float* bias;      // [E]
+  const float* stab;      // sigmoid table (bf16 logits), global
+  int32_t* packed;        // [T, k]
+  int32_t* counts;        // [NE]
+  int32_t* offsets;       // [NE + 1]
+  int32_t* perm;          // [T * k]
+  int32_t* ids;           // [T, k] or nullptr
+  int* err;               // device status word
+  int T, k, Kg, off, cnt, NE;
+  float scale;
+};
+
+// Per-warp shared scratch of the row routine.
+struct WarpScratch {
+  float b[kE];            // biased scores of the row
+  float pool[32];         // threshold pool
+  uint32_t skey[32];      // survivor keys
+  int32_t sid[32];        // survivor expert ids
+  int32_t slot_id[kMaxK]; // expert id of each slot
+};
+
+enum { DT_F32 = 0, DT_BF16 = 1 };
+
+template <int DT>
+__device__ __forceinline__ float row_sigmoid(const void* row, int e, const float* stab) {
+  if constexpr (DT == DT_BF16) {
+    return sig_bf16(stab, static_cast<const uint16_t*>(row)[e]);
+  } else {
+    return sig_f32(static_cast<const float*>(row)[e]);
+  }
+}
+
+// Loads this lane's 28 biases into registers.
+__device__ __forceinline__ void load_lane_bias(const float* __restrict__ bias, float (&bl)[kEPL]) {
+  const int lane = threadIdx.x & 31;
+  const float4* p = reinterpret_cast<const float4*>(bias + lane * kEPL);
+#pragma unroll
+  for (int q = 0; q < kEPL / 4; ++q) {
+    const float4 v = __ldg(p + q);
+    bl[4 * q + 0] = v.x;
+    bl[4 * q + 1] = v.y;
+    bl[4 * q + 2] = v.z;
+    bl[4 * q + 3] = v.w;
+  }
+}
+
+// Result of one routed row, valid in lanes j < k.
+struct SlotOut {
+  int32_t id;      // global expert id of slot j
+  int32_t lid;     // relabelled id (== id when cnt == 0)
+  int32_t packed;  // (lid << 16) | bf16 weight bits
+};
+
+// Routes one row.  `row` points to the row's E logits in shared memory (16-byte
+// aligned).  All 32 lanes must call it.
+template <int DT>
+__device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[kEPL],
+                                             const float* stab, const RouteArgs& a,
+                                             WarpScratch& ws) {
+  const unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int e0 = lane * kEPL;
+
+  // ---- a1, a2: scores, biased scores, lane top-2
+  float b[kEPL];
+  float lm1 = -INFINITY, lm2 = -INFINITY;
+  if constexpr (DT == DT_BF16) {
+    const uint2* p = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(row) + e0);
+#pragma unroll
+    for (int q = 0; q < kEPL / 4; ++q) {
+      const uint2 v = p[q];
+      const uint32_t h[4] = {v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float bb = __fadd_rn(sig_bf16(stab, h[r]), bl[4 * q + r]);
+        b[4 * q + r] = bb;
+        lm2 = fmaxf(lm2, fminf(lm1, bb));
+        lm1 = fmaxf(lm1, bb);
+      }
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(row) + e0);
+#pragma unroll
+    for (int q = 0; q < kEPL / 4; ++q) {
+      const float4 v = p[q];
+      const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float bb = __fadd_rn(sig_f32(x[r]), bl[4 * q + r]);
+        b[4 * q + r] = bb;
+        lm2 = fmaxf(lm2, fminf(lm1, bb));
+        lm1 = fmaxf(lm1, bb);
+      }
+    }
+  }
+  {
+    float4* d = reinterpret_cast<float4*>(ws.b + e0);
+#pragma unroll
+    for (int q = 0; q < kEPL / 4; ++q)
+      d[q] = make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+  }
+
+  // ---- a3: group score = sum of the group's two largest b (4-lane merge of top-2 lists)
+  float gm1 = lm1, gm2 = lm2;
+#pragma unroll
+  for (int o = 1; o < kLanesPerGroup; o <<= 1) {
+    const float p1 = __shfl_xor_sync(FULL, gm1, o);
+    const float p2 = __shfl_xor_sync(FULL, gm2, o);
+    const float n2 = fmaxf(fminf(gm1, p1), fmaxf(gm2, p2));
+    gm1 = fmaxf(gm1, p1);
+    gm2 = n2;
+  }
+  const float gs = __fadd_rn(gm1, gm2);
+
+  // ---- a4: keep the topk_group best groups, ties to the lower group index
+  const int my_g = lane / kLanesPerGroup;
+  int grank = 0;
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    const float o = __shfl_sync(FULL, gs, g * kLanesPerGroup);
+    grank += (o > gs || (o == gs && g < my_g)) ? 1 : 0;
+  }
+  const bool kept = grank < a.Kg;
+  const uint32_t kept_lanes = __ballot_sync(FULL, kept);
+  const int nk = __popc(kept_lanes);
+  const int ki = __popc(kept_lanes & ((1u << lane) - 1u));
+
+  // ---- a5: threshold from the pool of kept lanes' top-2
+  ws.pool[lane] = -INFINITY;
+  __syncwarp();
+  int pool_n;
+  if (2 * nk <= 32) {
+    if (kept) {
+      ws.pool[2 * ki] = lm1;
+      ws.pool[2 * ki + 1] = lm2;
+    }
+    pool_n = 2 * nk;
+  } else {
+    if (kept) {
+      ws.pool[ki] = lm1;
+      if (ki < 32 - nk) ws.pool[nk + ki] = lm2;
+    }
+    pool_n = 32;
+  }
+  __syncwarp();
+  float tau0 = -INFINITY;
+  if (pool_n >= a.k) {
+    float v = ws.pool[lane];
+    // bitonic sort, descending across lanes
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const float o = __shfl_xor_sync(FULL, v, stride);
+        const bool desc = (lane & size) == 0;
+        const bool lower = (lane & stride) == 0;
+        v = (lower == desc) ? fmaxf(v, o) : fminf(v, o);
+      }
+    }
+    tau0 = __shfl_sync(FULL, v, a.k - 1);
+  }
+
+  uint32_t smask = 0;
+  if (kept) {
+#pragma unroll
+    for (int i = 0; i < kEPL; ++i) smask |= (b[i] >= tau0) ? (1u << i) : 0u;
+  }
+  const int c = __popc(smask);
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += n;
+  }
+  const int total = __shfl_sync(FULL, incl, 31);
+  __syncwarp();  // ws.b visible to the warp
+
+  if (total <= 32) {
+    int pos = incl - c;
+    while (smask) {
+      const int i = __ffs(smask) - 1;
+      smask &= smask - 1u;
+      ws.skey[pos] = fkey(ws.b[e0 + i]);
+      ws.sid[pos] = e0 + i;
+      ++pos;
+    }
+    __syncwarp();
+    uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
+    const int my_id = (lane < total) ? ws.sid[lane] : 0;
+    for (int j = 0; j < a.k; ++j) {
+      const uint32_t top = __reduce_max_sync(FULL, key);
+      const int win = __ffs(__ballot_sync(FULL, key == top)) - 1;
+      if (lane == win) {
+        ws.slot_id[j] = my_id;
+        key = 0u;
+      }
+    }
+  } else {
+    // exact slow path: k rounds of (warp max over lane maxima), winner lane rescans
+    uint32_t taken = 0;
+    auto lane_best = [&](uint32_t& bk, int& bi) {
+      bk = 0u;
+      bi = -1;
+      if (!kept) return;
+      for (int i = 0; i < kEPL; ++i) {
+        if (taken & (1u << i)) continue;
+        const uint32_t kk = fkey(ws.b[e0 + i]);
+        if (kk > bk) {
+          bk = kk;
+          bi = i;
+        }
+      }
+    };
+    uint32_t bk;
+    int bi;
+    lane_best(bk, bi);
+    for (int j = 0; j < a.k; ++j) {
+      const uint32_t top = __reduce_max_sync(FULL, bk);
+      const int win = __ffs(__ballot_sync(FULL, bk == top)) - 1;
+      if (lane == win) {
+        ws.slot_id[j] = e0 + bi;
+        taken |= 1u << bi;
+        lane_best(bk, bi);
+      }
+    }
+  }
+  __syncwarp();
+
+  // ---- a6..a8: renormalise the unbiased scores, relabel, pack
+  SlotOut out;
+  out.id = 0;
+  out.lid = 0;
+  out.packed = 0;
+  float s = 0.0f;
+  if (lane < a.k) {
+    out.id = ws.slot_id[lane];
+    s = row_sigmoid<DT>(row, out.id, stab);
+  }
+  float den = 0.0f;
+  for (int j = 0; j < a.k; ++j) den = __fadd_rn(den, __shfl_sync(FULL, s, j));
+  if (lane < a.k) {
+    const float w = __fmul_rn(__fdiv_rn(s, den), a.scale);
+    const uint32_t wb = f32_to_bf16_bits(w);
+    int lid = out.id;
+    if (a.cnt > 0) lid = (out.id >= a.off && out.id < a.off + a.cnt) ? out.id - a.off : a.cnt + lane;
+    out.lid = lid;
+    out.packed = static_cast<int32_t>((static_cast<uint32_t>(lid) << 16) | wb);
+  }
+  __syncwarp();
+  return out;
+}
+
+// ---------------------------------------------------------------- block scan
+// Exclusive scan of in[0..n) into out[0..n], out[n] = total.  All threads of the
+// block call it; `tmp` holds at least 32 ints.  in and out may alias.
+__device__ __forceinline__ void block_exclusive_scan(const int* in, int* out, int n, int* tmp) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, wid = tid >> 5, nw = (nt + 31) >> 5;
+  const int per = (n + nt - 1) / nt;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += in[i];
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) tmp[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int v = (lane < nw) ? tmp[lane] : 0;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    if (lane < nw) tmp[lane] = inc - v;
+  }
+  __syncthreads();
+  int run = tmp[wid] + incl - sum;
+  __syncthreads();  // everyone has read tmp; in may alias out
+  for (int i = lo; i < hi; ++i) {
+    const int v = in[i];
+    out[i] = run;
+    run += v;
+  }
+  if (hi == n && lo < hi) out[n] = run;
+  if (n == 0 && tid == 0) out[0] = 0;
+  __syncthreads();
+}
+
+}  // namespace moe
