@@ -239,17 +239,18 @@ def decode_latency(torch, mr, dev, reps=200, replays=10):
                     mr.empty_kernel(ctas, stream=st)
         times = {}
         for name, g in (("route", g_route), ("empty", g_empty)):
-            g.replay()
-            torch.cuda.synchronize()
-            samples = []
-            for _ in range(replays):
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record(st)
+            with torch.cuda.stream(st):  # replay and time on the same stream
                 g.replay()
-                b.record(st)
-                b.synchronize()
-                samples.append(a.elapsed_time(b) * 1e3 / reps)
+                st.synchronize()
+                samples = []
+                for _ in range(replays):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(st)
+                    g.replay()
+                    b.record(st)
+                    b.synchronize()
+                    samples.append(a.elapsed_time(b) * 1e3 / reps)
             times[name] = statistics.median(samples)
         res["T"].append(T)
         res["us_per_call"].append(round(times["route"], 3))
@@ -266,6 +267,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed prefill steps only (no decode sweep, CPU baseline, end-to-end or "
+                         "clock probe): the command profiled under ncu")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -329,7 +333,7 @@ def main():
     # The timed region may be too short for 50 ms clock samples; then sample a 1 s run of
     # the same kernel right after it and say so.
     n_inside = sum(1 for ts, _ in sampler.lines if sampler.t0 <= ts <= sampler.t1)
-    probe = n_inside < 3
+    probe = n_inside < 3 and not args.quick
     if probe:
         sampler.mark(0)
         t_probe = time.time()
@@ -354,10 +358,10 @@ def main():
     h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()
              if v is not None}
     d_in = bufs[0]
-    e2e_steps = max(3, min(args.steps, 100))
+    e2e_steps = 0 if args.quick else max(3, min(args.steps, 100))
     h2d = h_in.numel() * 2
     d2h = sum(v.numel() * v.element_size() for v in h_out.values())
-    for _ in range(2):
+    for _ in range(2 if e2e_steps else 0):
         d_in.view(torch.int16).copy_(h_in, non_blocking=True)
         mr.route(d_in, bias, out=outs[0])
         for k2, v in h_out.items():
@@ -373,14 +377,14 @@ def main():
             v.copy_(outs[0][k2], non_blocking=True)
     eb.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = ea.elapsed_time(eb) / e2e_steps
+    e2e_ms = ea.elapsed_time(eb) / max(1, e2e_steps)
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt[0])
 
     decode = None
-    if rank == 0 and not args.no_decode:
+    if rank == 0 and not (args.no_decode or args.quick):
         decode = decode_latency(torch, mr, dev)
 
     peaks, peak_src = measured_peaks()
@@ -407,14 +411,15 @@ def main():
                      "kernel": "k_route_prefill<bf16>", "algorithmic_bytes": ab,
                      "kernel_us": kernel_ms * 1e3, "peak_source": f"{peak_src} hbm_gbs (copy)"},
         "clocks": clocks,
-        "e2e": {"value": world * T_PREFILL / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "e2e": ({"value": world * T_PREFILL / (e2e_ms * 1e-3), "unit": "tokens/s",
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+                if e2e_steps else None),
         "gpu_launches": args.steps,
         "device_status": status, "invariants_ok": ok,
     }
     if decode is not None:
         line["decode"] = decode
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not (args.no_cpu_baseline or args.quick):
         line["cpu_baseline"] = cpu_baseline()
     if world > 1:
         dist.destroy_process_group()

@@ -18,6 +18,7 @@ struct DevState {
   int nsm = 0;
   int blocks_per_sm = 0;
   float* stab = nullptr;  // sigmoid table for bf16 logits
+  float2* etab = nullptr; // 2^(j/64) table for float32 logits
   int* err = nullptr;     // device status word
   PrefillWS pw = {};
   int* pw_block = nullptr;
@@ -46,8 +47,9 @@ int init_device(DevState& d) {
   const int grid_max = d.nsm * d.blocks_per_sm;
   const size_t n_tab = size_t(kSigTablePad);
   const size_t n_hist = size_t(kMaxBins) * grid_max;
-  // one block: [table][hist][prefix][counts][bar x2, err, pad]
-  const size_t bytes = n_tab * 4 + 2 * n_hist * 4 + size_t(kMaxBins) * 4 + 64;
+  // one block: [sigmoid table][exp table][hist][prefix][counts][bar x2, err, pad]
+  const size_t n_etab = size_t(2 * kExpTable);
+  const size_t bytes = (n_tab + n_etab) * 4 + 2 * n_hist * 4 + size_t(kMaxBins) * 4 + 64;
   int* blk = nullptr;
   if (cudaMalloc(&blk, bytes) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaMemset(blk, 0, bytes) != cudaSuccess) {
@@ -56,13 +58,14 @@ int init_device(DevState& d) {
   }
   d.pw_block = blk;
   d.stab = reinterpret_cast<float*>(blk);
-  d.pw.hist = blk + n_tab;
+  d.etab = reinterpret_cast<float2*>(blk + n_tab);
+  d.pw.hist = blk + n_tab + n_etab;
   d.pw.prefix = d.pw.hist + n_hist;
   d.pw.counts = d.pw.prefix + n_hist;
   d.pw.bar = reinterpret_cast<unsigned*>(d.pw.counts + kMaxBins);
   d.err = reinterpret_cast<int*>(d.pw.bar + 2);
   d.pw.grid_max = grid_max;
-  if (launch_sigmoid_table(d.stab, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (launch_sigmoid_table(d.stab, d.etab, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
   d.ready = true;
   return MOE_ROUTE_OK;
@@ -138,6 +141,7 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
   a.logits = logits;
   a.bias = bias;
   a.stab = d->stab;
+  a.etab = d->etab;
   a.packed = packed;
   a.counts = counts;
   a.offsets = offsets;
@@ -206,7 +210,7 @@ int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream
   DevState* d = nullptr;
   const int rc = get_state(st, &d);
   if (rc != MOE_ROUTE_OK) return rc;
-  return launch_sigmoid(x, dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32, d->stab, s, n, st) ==
+  return launch_sigmoid(x, dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32, d->stab, d->etab, s, n, st) ==
                  cudaSuccess
              ? MOE_ROUTE_OK
              : MOE_ROUTE_E_CUDA;

@@ -18,9 +18,9 @@ struct PrefillWS {
 
 constexpr int kSigTablePad = (kSigTable + 3) / 4 * 4;  // table length rounded to 16 bytes
 
-cudaError_t launch_sigmoid_table(float* tab, cudaStream_t st);
-cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, float* s, int n,
-                           cudaStream_t st);
+cudaError_t launch_sigmoid_table(float* tab, float2* etab, cudaStream_t st);
+cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const float2* etab, float* s,
+                           int n, cudaStream_t st);
 cudaError_t setup_decode_kernels();
 cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_empty(int ctas, cudaStream_t st);

@@ -126,8 +126,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
 }
 
 // --------------------------------------------------------------- sigmoid table
-__global__ void k_sigmoid_table(float* tab) {
+__global__ void k_sigmoid_table(float* tab, float2* etab) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < kExpTable) {
+    const double v = exp2(static_cast<double>(i) / kExpTable);
+    const float hi = __double2float_rn(v);
+    etab[i] = make_float2(hi, __double2float_rn(v - static_cast<double>(hi)));
+  }
   if (i >= kSigTablePad) return;
   if (i >= kSigTable) {
     tab[i] = 0.0f;
@@ -141,23 +146,24 @@ __global__ void k_sigmoid_table(float* tab) {
   tab[i] = __double2float_rn(s);
 }
 
-__global__ void k_sigmoid(const void* x, int dtype, const float* __restrict__ tab, float* s, int n) {
+__global__ void k_sigmoid(const void* x, int dtype, const float* __restrict__ tab,
+                          const float2* __restrict__ etab, float* s, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     s[i] = (dtype == DT_BF16) ? sig_bf16(tab, static_cast<const uint16_t*>(x)[i])
-                              : sig_f32(static_cast<const float*>(x)[i]);
+                              : sig_f32(static_cast<const float*>(x)[i], etab);
   }
 }
 
-cudaError_t launch_sigmoid_table(float* tab, cudaStream_t st) {
-  k_sigmoid_table<<<(kSigTablePad + 255) / 256, 256, 0, st>>>(tab);
+cudaError_t launch_sigmoid_table(float* tab, float2* etab, cudaStream_t st) {
+  k_sigmoid_table<<<(kSigTablePad + 255) / 256, 256, 0, st>>>(tab, etab);
   return cudaGetLastError();
 }
 
-cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, float* s, int n,
-                           cudaStream_t st) {
+cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const float2* etab, float* s,
+                           int n, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   const int blocks = min((n + 255) / 256, 4096);
-  k_sigmoid<<<blocks, 256, 0, st>>>(x, dtype, tab, s, n);
+  k_sigmoid<<<blocks, 256, 0, st>>>(x, dtype, tab, etab, s, n);
   return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@ struct RouteArgs {
   const void* logits;     // [T, E] f32 or bf16 bits
   const float* bias;      // [E]
   const float* stab;      // sigmoid table (bf16 logits), global
+  const float2* etab;     // 2^(j/64) float-float table (float32 logits), global
   int32_t* packed;        // [T, k]
   int32_t* counts;        // [NE]
   int32_t* offsets;       // [NE + 1]
@@ -44,11 +45,12 @@ struct WarpScratch {
 enum { DT_F32 = 0, DT_BF16 = 1 };
 
 template <int DT>
-__device__ __forceinline__ float row_sigmoid(const void* row, int e, const float* stab) {
+__device__ __forceinline__ float row_sigmoid(const void* row, int e, const float* stab,
+                                             const float2* etab) {
   if constexpr (DT == DT_BF16) {
     return sig_bf16(stab, static_cast<const uint16_t*>(row)[e]);
   } else {
-    return sig_f32(static_cast<const float*>(row)[e]);
+    return sig_f32(static_cast<const float*>(row)[e], etab);
   }
 }
 
@@ -108,7 +110,7 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
       const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float bb = __fadd_rn(sig_f32(x[r]), bl[4 * q + r]);
+        const float bb = __fadd_rn(sig_f32(x[r], a.etab), bl[4 * q + r]);
         b[4 * q + r] = bb;
         lm2 = fmaxf(lm2, fminf(lm1, bb));
         lm1 = fmaxf(lm1, bb);
@@ -256,7 +258,7 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   float s = 0.0f;
   if (lane < a.k) {
     out.id = ws.slot_id[lane];
-    s = row_sigmoid<DT>(row, out.id, stab);
+    s = row_sigmoid<DT>(row, out.id, stab, a.etab);
   }
   float den = 0.0f;
   for (int j = 0; j < a.k; ++j) den = __fadd_rn(den, __shfl_sync(FULL, s, j));

@@ -62,7 +62,8 @@ def test_sigmoid_bf16_every_value(mr):
     assert bad.size == 0, (bad[:5], xs[np.isfinite(xs)][bad[:5]])
 
 
-def test_sigmoid_f32_within_2ulp(mr):
+def test_sigmoid_f32_within_1ulp(mr):
+    """float32 logits: within one ulp of the oracle everywhere, equal almost everywhere."""
     x = np.concatenate([gen.uniform_f32(11, 1 << 20, -40.0, 40.0), gen.normal_f32(12, 1 << 20),
                         gen.normal_f32(13, 1 << 18) * np.float32(1e-4),
                         gen.uniform_f32(14, 1 << 16, -104.0, -80.0)]).astype(np.float32)
@@ -71,7 +72,16 @@ def test_sigmoid_f32_within_2ulp(mr):
     d = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
     frac_exact = float((d == 0).mean())
     print("f32 sigmoid: max ulp", int(d.max()), "fraction exact", frac_exact)
-    assert d.max() <= 2
+    bad = np.nonzero(d)[0]
+    if bad.size:
+        import oracle_pins
+        for i in bad[:: max(1, bad.size // 12)][:12]:
+            exact, near = oracle_pins.exact_sigmoid_f32(float(x[i]))
+            print(f"x={x[i]!r} gpu={got[i]!r} oracle={want[i]!r} exact={exact!r} near_mid={near}")
+        ranges = np.histogram(x[bad], bins=[-200, -87.4, -20, -1, -1e-3, 0, 1e-3, 1, 20, 200])[0]
+        print("mismatches by x range", ranges.tolist())
+    assert d.max() <= 1
+    assert frac_exact >= 0.9999
 
 
 # ------------------------------------------------------------- full routing
