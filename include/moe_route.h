@@ -142,6 +142,39 @@ int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream
 int moe_route_set_path(int path);
 
 /*
+ * moe_route_noalloc -- moe_route for callers that cannot allocate device memory.
+ * The pages describe no counterpart: this is a deployment variant of the same
+ * routing kernels, not a step of the method.
+ *
+ * moe_route obtains its workspace with cudaMalloc on first use.  A caller that has
+ * reserved all free HBM up front (a serving engine's weights and KV cache), runs under
+ * a memory pool that forbids raw allocations, or may only touch the buffers it is
+ * given, uses this entry point instead: it never calls cudaMalloc, cudaFree or any
+ * allocating routine.  Its scratch is a fixed array in the library's device image,
+ * about 1.4 MB, held by every GPU that loads the library until the process exits.
+ *   - Arguments, outputs and results are those of moe_route.  It always runs the
+ *     persistent multi-CTA kernel (T = 0 writes zero counts and offsets only).
+ *   - status: nullable DEVICE pointer to one int32 the call sets to 0, then to
+ *     MOE_ROUTE_E_DEVICE_TIMEOUT if a bounded device-side wait runs out.  With NULL,
+ *     such an error is recorded only inside the library's array.
+ *   - Limits: at most 1056 expert bins (any supported E, k and local_count fits) and
+ *     at most 160 CTAs (a larger GPU runs 160); bins beyond the limit return
+ *     MOE_ROUTE_E_UNSUPPORTED.
+ *   - The first call on each device (with that device current) looks up the array's
+ *     address, writes the score tables into it and waits for the device; make that
+ *     first call before any stream capture (during capture it returns
+ *     MOE_ROUTE_E_WORKSPACE and enqueues nothing).
+ *   - Every call shares the one array and it keeps the last call's contents; each call
+ *     zeroes the words that must start at zero.  Calls that overlap on the GPU (other
+ *     streams, other threads) race on the array and must be serialised by the caller.
+ */
+int moe_route_noalloc(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+                      int n_group, int topk_group, float scale, int local_offset,
+                      int local_count, int32_t* packed, int32_t* counts, int32_t* offsets,
+                      int32_t* perm, int32_t* topk_ids, int32_t* status,
+                      struct CUstream_st* stream);
+
+/*
  * Measurement helper: enqueues one launch of an empty kernel with the decode kernel's
  * launch shape (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 8).  Replayed in a
  * CUDA graph it gives the launch-latency floor that decode routing is compared with.

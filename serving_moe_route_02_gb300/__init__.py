@@ -61,6 +61,8 @@ def load(path: str | None = None):
     lib.moe_route_sigmoid.restype = I
     lib.moe_route_set_path.argtypes = [I]
     lib.moe_route_set_path.restype = I
+    lib.moe_route_noalloc.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
+    lib.moe_route_noalloc.restype = I
     lib.moe_route_empty.argtypes = [I, P]
     lib.moe_route_empty.restype = I
     lib.moe_route_strerror.argtypes = [I]
@@ -148,6 +150,22 @@ def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int
                           _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]),
                           _ptr(out.get("ids")), _stream(stream))
     _check(rc, "moe_route")
+    return out
+
+
+def route_noalloc(logits: torch.Tensor, bias: torch.Tensor, *, out: dict, status=None,
+                  k: int = 16, n_group: int = 8, topk_group: int = 4, scale: float = 2.5,
+                  local_offset: int = 0, local_count: int = 0, stream=None) -> dict:
+    """moe_route_noalloc: the same routing with scratch in the library's static device
+    array, for callers that cannot allocate.  `out` (see alloc_outputs) must be given;
+    `status` is an optional one-element int32 CUDA tensor for device-side errors."""
+    T, E = logits.shape
+    rc = load().moe_route_noalloc(_ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group,
+                                  topk_group, float(scale), local_offset, local_count,
+                                  _ptr(out["packed"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+                                  _ptr(out["perm"]), _ptr(out.get("ids")), _ptr(status),
+                                  _stream(stream))
+    _check(rc, "moe_route_noalloc")
     return out
 
 
