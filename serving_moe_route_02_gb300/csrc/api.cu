@@ -22,6 +22,7 @@ struct DevState {
   int* err = nullptr;     // device status word
   PrefillWS pw = {};
   int* pw_block = nullptr;
+  float* glogits = nullptr;  // [64][E] fp32 logits of the fused contraction when none given
 };
 
 constexpr int kMaxDevices = 64;
@@ -47,9 +48,12 @@ int init_device(DevState& d) {
   const int grid_max = d.nsm * d.blocks_per_sm;
   const size_t n_tab = size_t(kSigTablePad);
   const size_t n_hist = size_t(kMaxBins) * grid_max;
-  // one block: [sigmoid table][exp table][hist][prefix][counts][bar x2, err, pad]
+  if (setup_router_gemm() != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  // one block: [sigmoid table][exp table][hist][prefix][counts][bar x2, err, pad][logits]
   const size_t n_etab = size_t(2 * kExpTable);
-  const size_t bytes = (n_tab + n_etab) * 4 + 2 * n_hist * 4 + size_t(kMaxBins) * 4 + 64;
+  const size_t n_log = size_t(64) * kE;
+  const size_t bytes = (n_tab + n_etab) * 4 + 2 * n_hist * 4 + size_t(kMaxBins) * 4 + 64 +
+                       n_log * 4;
   int* blk = nullptr;
   if (cudaMalloc(&blk, bytes) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaMemset(blk, 0, bytes) != cudaSuccess) {
@@ -64,6 +68,7 @@ int init_device(DevState& d) {
   d.pw.counts = d.pw.prefix + n_hist;
   d.pw.bar = reinterpret_cast<unsigned*>(d.pw.counts + kMaxBins);
   d.err = reinterpret_cast<int*>(d.pw.bar + 2);
+  d.glogits = reinterpret_cast<float*>(d.pw.bar + 16);
   d.pw.grid_max = grid_max;
   if (launch_sigmoid_table(d.stab, d.etab, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
@@ -180,10 +185,42 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
                           int local_offset, int local_count, float* logits_out, int32_t* packed,
                           int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* topk_ids,
                           struct CUstream_st* stream) {
-  (void)hidden; (void)w_router; (void)bias; (void)T; (void)H; (void)E; (void)k; (void)n_group;
-  (void)topk_group; (void)scale; (void)local_offset; (void)local_count; (void)logits_out;
-  (void)packed; (void)counts; (void)offsets; (void)perm; (void)topk_ids; (void)stream;
-  return MOE_ROUTE_E_UNSUPPORTED;
+  int rc = check_route_args(T, E, k, n_group, topk_group, local_offset, local_count);
+  if (rc != MOE_ROUTE_OK) return rc;
+  if (T < 1 || H <= 0) return MOE_ROUTE_E_INVALID_ARG;
+  if (!hidden || !w_router || !bias || !packed || !counts || !offsets || !perm)
+    return MOE_ROUTE_E_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(hidden) % 16 != 0 || reinterpret_cast<uintptr_t>(w_router) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(bias) % 16 != 0 || reinterpret_cast<uintptr_t>(logits_out) % 16 != 0)
+    return MOE_ROUTE_E_INVALID_ARG;
+  if (T > 64 || H % 64 != 0) return MOE_ROUTE_E_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevState* d = nullptr;
+  rc = get_state(st, &d);
+  if (rc != MOE_ROUTE_OK) return rc;
+  if ((H / 64) % router_gemm_cluster() != 0) return MOE_ROUTE_E_UNSUPPORTED;
+  float* logits = logits_out ? logits_out : d->glogits;
+  if (launch_router_gemm(hidden, w_router, logits, T, H, E, d->err, st) != cudaSuccess)
+    return MOE_ROUTE_E_CUDA;
+  RouteArgs a = {};
+  a.logits = logits;
+  a.bias = bias;
+  a.stab = d->stab;
+  a.etab = d->etab;
+  a.packed = packed;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.ids = topk_ids;
+  a.err = d->err;
+  a.T = T;
+  a.k = k;
+  a.Kg = topk_group;
+  a.off = local_offset;
+  a.cnt = local_count;
+  a.NE = bins(E, k, local_count);
+  a.scale = scale;
+  return launch_route_decode(a, DT_F32, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }
 
 int moe_route_device_status(void) {

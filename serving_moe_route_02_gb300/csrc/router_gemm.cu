@@ -1,0 +1,315 @@
+// router_gemm.cu -- step a0: logits[t][e] = sum_h hidden[t][h] * W[e][h] for decode
+// batches (T <= 64), bf16 operands, fp32 accumulation, on the 5th-generation tensor
+// cores; the routing kernel then runs on the fp32 logits.
+//
+// The router weight (896 x 7168 bf16, 12.85 MB) dominates the traffic: at T <= 64 the
+// contraction does at most ~64 flop per weight byte, so it is bound by reading W once.
+// Layout of the work (swap-AB, so the experts fill the MMA's M = 128 and the few
+// tokens its N = T rounded up to 16):
+//   grid = 7 expert tiles x C K-splits, one thread-block cluster of C CTAs per tile
+//   (C = 16 when the GPU schedules such clusters, else 8);
+//   each CTA streams its 128 x (7168 / C) slice of W and the matching hidden columns
+//   with 2-D TMA loads (128-byte swizzle) into a ring of shared-memory stages, one
+//   thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) into a 128 x N
+//   accumulator in tensor memory, and tcgen05.commit frees each stage;
+//   the 4 warps read the accumulator (tcgen05.ld), stage it in shared memory, and the
+//   cluster reduce-scatters the C partial tiles through distributed shared memory,
+//   summing in a fixed order (deterministic), each CTA writing 128 / C experts.
+// All mbarrier waits are bounded; tensor memory is released on every path.
+#include <cuda.h>
+#include <cooperative_groups.h>
+
+#include "launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace moe {
+
+constexpr int kGemmThreads = 128;
+constexpr int kBM = 128;               // experts per tile (MMA M)
+constexpr int kBK = 64;                // K per stage: one 128-byte swizzle row of bf16
+constexpr int kStageW = kBM * kBK * 2; // 16 KB
+constexpr int kStageH = 64 * kBK * 2;  // room for N <= 64 token rows: 8 KB
+constexpr int kStage = kStageW + kStageH;
+constexpr int kMaxStages = 7;
+constexpr int kTmemCols = 64;
+constexpr int kPartStride = 64 + 1;    // padded row of the staged fp32 partial tile
+
+struct GemmArgs {
+  float* logits;  // [T, E] fp32 out
+  int T, Tpad, E;
+  int kb_per_cta; // 64-wide K blocks per CTA
+  int stages;     // ring depth
+  int* err;
+};
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  // tcgen05 shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+  // groups 1024 bytes apart (stride byte offset), descriptor version 1.
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(16 >> 4) << 16;    // leading byte offset (unused for swizzled K-major)
+  d |= uint64_t(1024 >> 4) << 32;  // stride byte offset
+  d |= uint64_t(1) << 46;          // version
+  d |= uint64_t(2) << 61;          // SWIZZLE_128B
+  return d;
+}
+
+__device__ __forceinline__ uint32_t mma_idesc(int n) {
+  // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, M = 128, N = n
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_router_gemm(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
+                  GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled stages
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int r = static_cast<int>(cluster.block_rank());
+  const int mtile = blockIdx.x / C;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = g.stages;
+
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMaxStages * kStage);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* done = empty + kMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  float* part = reinterpret_cast<float*>(stages);  // reused after the MMAs complete
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *tmem_slot;
+  const int kb0 = r * g.kb_per_cta;
+  const uint32_t stage_bytes = uint32_t(kStageW + g.Tpad * kBK * 2);
+
+  if (threadIdx.x == 0) {
+    // producer: TMA loads of W and hidden tiles into the ring
+    for (int kb = 0; kb < g.kb_per_cta; ++kb) {
+      const int s = kb % NS;
+      if (kb >= NS && !mbar_wait_bounded(empty + s, uint32_t((kb / NS - 1) & 1), g.err)) break;
+      uint8_t* st = stages + s * kStage;
+      mbar_expect_tx(full + s, stage_bytes);
+      const int k = (kb0 + kb) * kBK;
+      tma_load_2d(smem_addr(st), &tmW, k, mtile * kBM, smem_addr(full + s));
+      tma_load_2d(smem_addr(st + kStageW), &tmH, k, 0, smem_addr(full + s));
+    }
+  } else if (threadIdx.x == 32) {
+    // MMA issuer: 4 MMAs of K = 16 per 64-wide stage
+    const uint32_t idesc = mma_idesc(g.Tpad);
+    bool ok = true;
+    for (int kb = 0; kb < g.kb_per_cta && ok; ++kb) {
+      const int s = kb % NS;
+      if (!mbar_wait_bounded(full + s, uint32_t((kb / NS) & 1), g.err)) {
+        ok = false;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      uint8_t* st = stages + s * kStage;
+      const uint64_t ad = sw128_desc(smem_addr(st));
+      const uint64_t bd = sw128_desc(smem_addr(st + kStageW));
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k)
+        mma_bf16(tmem, ad + uint64_t(2 * k), bd + uint64_t(2 * k), idesc, (kb | k) != 0);
+      mma_commit(smem_addr(empty + s));
+    }
+    mma_commit(smem_addr(done));  // arrives once every MMA issued above has completed
+  }
+  __syncwarp();
+
+  // ---- epilogue: accumulator rows -> shared memory
+  const bool acc_ok = mbar_wait_bounded(done, 0, g.err);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (acc_ok) {
+    uint32_t v[64];
+    const uint32_t ta = tmem + (uint32_t(warp * 32) << 16);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%"
+        "15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%"
+        "38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%"
+        "61,%62,%63}, [%64];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+          "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]), "=r"(v[37]),
+          "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]), "=r"(v[43]),
+          "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]),
+          "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
+          "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]),
+          "=r"(v[62]), "=r"(v[63])
+        : "r"(ta)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    float* prow = part + (warp * 32 + lane) * kPartStride;
+#pragma unroll
+    for (int c = 0; c < 64; ++c) prow[c] = __uint_as_float(v[c]);
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  cluster.sync();
+
+  // ---- reduce-scatter over the cluster: CTA r sums rows [r R, r R + R) of all C partials
+  const int R = kBM / C;
+  for (int idx = threadIdx.x; idx < R * g.T; idx += kGemmThreads) {
+    const int t = idx / R, i = idx - t * R;
+    const int row = r * R + i;
+    float acc = 0.0f;
+    for (int c = 0; c < C; ++c) {
+      const float* rp = cluster.map_shared_rank(part, c);
+      acc = __fadd_rn(acc, rp[row * kPartStride + t]);
+    }
+    const int e = mtile * kBM + row;
+    if (e < g.E) g.logits[size_t(t) * g.E + e] = acc;
+  }
+  cluster.sync();  // keep this CTA's partial tile alive for remote readers
+}
+
+// ------------------------------------------------------------------- host side
+namespace {
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled g_encode = nullptr;
+int g_cluster = 0;
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+              uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+constexpr int kGemmSmem = kMaxStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(kMaxStages * kStage >= kBM * kPartStride * 4, "partial tile must fit the ring");
+static_assert(kGemmSmem <= 227 * 1024, "router contraction smem exceeds 227 KB");
+
+}  // namespace
+
+cudaError_t setup_router_gemm() {
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || fn == nullptr || q != cudaDriverEntryPointSuccess)
+      return e != cudaSuccess ? e : cudaErrorNotSupported;
+    g_encode = reinterpret_cast<EncodeTiled>(fn);
+  }
+  cudaError_t e =
+      cudaFuncSetAttribute(k_router_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  // prefer clusters of 16 K-splits when the GPU can schedule 7 of them at once
+  g_cluster = 8;
+  if (cudaFuncSetAttribute(k_router_gemm, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+      cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(7 * 16, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, k_router_gemm, &cfg) == cudaSuccess &&
+        nclusters >= 7)
+      g_cluster = 16;
+  }
+  cudaGetLastError();  // clear a refused query
+  return cudaSuccess;
+}
+
+int router_gemm_cluster() { return g_cluster; }
+
+cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float* logits, int T,
+                               int H, int E, int* err, cudaStream_t st) {
+  const int Tpad = (T + 15) / 16 * 16;
+  const int C = g_cluster;
+  const int nkb = H / kBK;
+  if (Tpad > 64 || nkb % C != 0 || E % kBM != 0) return cudaErrorInvalidValue;
+  CUtensorMap tmW, tmH;
+  if (!make_map(&tmW, w, uint64_t(H), uint64_t(E), kBK, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&tmH, hidden, uint64_t(H), uint64_t(T), kBK, uint32_t(Tpad)))
+    return cudaErrorInvalidValue;
+  GemmArgs g = {};
+  g.logits = logits;
+  g.T = T;
+  g.Tpad = Tpad;
+  g.E = E;
+  g.kb_per_cta = nkb / C;
+  g.stages = g.kb_per_cta < kMaxStages ? g.kb_per_cta : kMaxStages;
+  g.err = err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((E / kBM) * C, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_router_gemm, tmW, tmH, g);
+}
+
+}  // namespace moe

@@ -1,0 +1,78 @@
+"""Fused router contraction + routing (moe_router_gemm_route) against the oracle.
+
+Logits: |gpu - ref| <= 1e-3 * max(|ref|, 1e-2 * max_row |ref|), ref accumulated in
+double.  Routing: the oracle router applied to the GPU's own float32 logits must give
+the GPU's packed ids, counts, offsets and permutation bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mr():
+    import serving_moe_route_02_gb300 as mr
+    mr.load()
+    mr.reserve()
+    return mr
+
+
+@pytest.fixture(scope="module")
+def weight():
+    cfg = gen.cfg2(1)
+    return cfg["w"], torch.from_numpy(cfg["w"].view(np.int16)).cuda()
+
+
+def logits_close(got, ref):
+    scale = np.maximum(np.abs(ref), 1e-2 * np.abs(ref).max(axis=1, keepdims=True))
+    err = np.abs(got.astype(np.float64) - ref) / scale
+    return float(err.max())
+
+
+@pytest.mark.parametrize("T", [1, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("off,cnt", [(0, 0), (0, 112)])
+def test_router_gemm_route(mr, weight, T, off, cnt):
+    w_np, w_dev = weight
+    cfg = gen.cfg2(T, off=off, cnt=cnt)
+    hid = torch.from_numpy(cfg["hidden"].view(np.int16)).cuda()
+    bias = torch.from_numpy(cfg["bias"]).cuda()
+    out = mr.router_gemm_route(hid, w_dev, bias, local_offset=off, local_count=cnt, want_ids=True)
+    torch.cuda.synchronize()
+    assert mr.device_status() == 0
+    logits = out["logits"].cpu().numpy()
+    ref = oracle.router_gemm(cfg["hidden"], w_np)
+    rel = logits_close(logits, ref)
+    print(f"T={T} max relative logit error {rel:.2e}")
+    assert rel <= 1e-3
+    rcfg = dict(logits=logits, dtype="f32", bias=cfg["bias"], T=T, E=896, k=16, G=8, Kg=4,
+                scale=2.5, off=off, cnt=cnt)
+    o = oracle.route_cfg(rcfg)
+    g = {k: v.cpu().numpy() for k, v in out.items() if v is not None and k != "logits"}
+    parity.compare(g, o, rcfg, exact=True)
+
+
+def test_router_gemm_without_logits_out(mr, weight):
+    w_np, w_dev = weight
+    cfg = gen.cfg2(16)
+    hid = torch.from_numpy(cfg["hidden"].view(np.int16)).cuda()
+    bias = torch.from_numpy(cfg["bias"]).cuda()
+    a = mr.router_gemm_route(hid, w_dev, bias, want_logits=True)
+    b = mr.router_gemm_route(hid, w_dev, bias, want_logits=False)
+    torch.cuda.synchronize()
+    for key in ("packed", "counts", "offsets", "perm"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_router_gemm_rejects(mr, weight):
+    _, w_dev = weight
+    hid = torch.zeros((65, 7168), dtype=torch.int16, device="cuda")
+    bias = torch.zeros(896, dtype=torch.float32, device="cuda")
+    with pytest.raises(mr.MoeRouteError) as e:
+        mr.router_gemm_route(hid, w_dev, bias)
+    assert e.value.status == mr.E_UNSUPPORTED
