@@ -259,6 +259,76 @@ def decode_latency(torch, mr, dev, reps=200, replays=10):
     return res
 
 
+def gemm_route_latency(torch, mr, dev, reps=100, replays=10):
+    """moe_router_gemm_route (contraction + routing, global ids) under CUDA-graph replay:
+    µs per call and the weight-read bandwidth it implies."""
+    cfg = gen.cfg2(1)
+    w = torch.from_numpy(cfg["w"].view(np.int16)).to(dev)
+    bias = torch.from_numpy(cfg["bias"]).to(dev)
+    res = {"T": [], "us_per_call": [], "weight_gbs": []}
+    st = torch.cuda.Stream(device=dev)
+    for T in (1, 4, 8, 16, 32, 64):
+        hid = torch.from_numpy(gen.cfg2(T)["hidden"].view(np.int16)).to(dev)
+        out = mr.alloc_outputs(T, E, K, 0, dev)
+        out["logits"] = torch.empty((T, E), dtype=torch.float32, device=dev)
+        with torch.cuda.stream(st):
+            mr.router_gemm_route(hid, w, bias, out=out, stream=st)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for _ in range(reps):
+                    mr.router_gemm_route(hid, w, bias, out=out, stream=st)
+            g.replay()
+            st.synchronize()
+            samples = []
+            for _ in range(replays):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                g.replay()
+                b.record(st)
+                b.synchronize()
+                samples.append(a.elapsed_time(b) * 1e3 / reps)
+        us = statistics.median(samples)
+        res["T"].append(T)
+        res["us_per_call"].append(round(us, 3))
+        res["weight_gbs"].append(round((E * 7168 * 2 + T * 7168 * 2) / (us * 1e-6) / 1e9, 1))
+    return res
+
+
+def run_case(torch, mr, dev, args, T=64):
+    """Plain launches of one decode-size path, for ncu captures."""
+    if args.case == "decode":
+        cfg = gen.cfg1(T)
+        lg = to_dev_bf16(torch, cfg["logits"], dev)
+        bias = torch.from_numpy(cfg["bias"]).to(dev)
+        out = mr.alloc_outputs(T, E, K, 112, dev)
+        step = lambda: mr.route(lg, bias, local_offset=336, local_count=112, out=out)  # noqa: E731
+    else:
+        cfg = gen.cfg2(T)
+        w = torch.from_numpy(cfg["w"].view(np.int16)).to(dev)
+        hid = torch.from_numpy(cfg["hidden"].view(np.int16)).to(dev)
+        bias = torch.from_numpy(cfg["bias"]).to(dev)
+        out = mr.alloc_outputs(T, E, K, 0, dev)
+        out["logits"] = torch.empty((T, E), dtype=torch.float32, device=dev)
+        step = lambda: mr.router_gemm_route(hid, w, bias, out=out)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    status = mr.device_status()
+    print(json.dumps({"case": args.case, "T": T, "steps": args.steps,
+                      "us_per_call_plain_launches": a.elapsed_time(b) * 1e3 / args.steps,
+                      "device_status": status}))
+    return 0 if status == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -267,6 +337,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--case", default=None, choices=["decode", "gemm"],
+                    help="run only --steps plain launches of one path (decode routing at 64 "
+                         "rows, or contraction + routing at 64 rows) and print a one-line "
+                         "summary: the commands profiled under ncu")
     ap.add_argument("--quick", action="store_true",
                     help="timed prefill steps only (no decode sweep, CPU baseline, end-to-end or "
                          "clock probe): the command profiled under ncu")
@@ -289,6 +363,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     mr.load()
     mr.reserve()
+    if args.case is not None:
+        return run_case(torch, mr, dev, args)
 
     cfg = gen.cfg3(T_PREFILL)
     host_logits = np.ascontiguousarray(cfg["logits"])
@@ -383,9 +459,10 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt[0])
 
-    decode = None
+    decode = gemm = None
     if rank == 0 and not (args.no_decode or args.quick):
         decode = decode_latency(torch, mr, dev)
+        gemm = gemm_route_latency(torch, mr, dev)
 
     peaks, peak_src = measured_peaks()
     ab = algorithmic_bytes(T_PREFILL)
@@ -419,6 +496,8 @@ def main():
     }
     if decode is not None:
         line["decode"] = decode
+    if gemm is not None:
+        line["router_gemm_route"] = gemm
     if rank == 0 and not (args.no_cpu_baseline or args.quick):
         line["cpu_baseline"] = cpu_baseline()
     if world > 1:

@@ -22,7 +22,7 @@ struct DevState {
   int* err = nullptr;     // device status word
   PrefillWS pw = {};
   int* pw_block = nullptr;
-  float* glogits = nullptr;  // [64][E] fp32 logits of the fused contraction when none given
+  float* gscores = nullptr;  // [64][E] fp32 scores written by the fused contraction
 };
 
 constexpr int kMaxDevices = 64;
@@ -68,7 +68,7 @@ int init_device(DevState& d) {
   d.pw.counts = d.pw.prefix + n_hist;
   d.pw.bar = reinterpret_cast<unsigned*>(d.pw.counts + kMaxBins);
   d.err = reinterpret_cast<int*>(d.pw.bar + 2);
-  d.glogits = reinterpret_cast<float*>(d.pw.bar + 16);
+  d.gscores = reinterpret_cast<float*>(d.pw.bar + 16);
   d.pw.grid_max = grid_max;
   if (launch_sigmoid_table(d.stab, d.etab, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
@@ -199,11 +199,11 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
   rc = get_state(st, &d);
   if (rc != MOE_ROUTE_OK) return rc;
   if ((H / 64) % router_gemm_cluster() != 0) return MOE_ROUTE_E_UNSUPPORTED;
-  float* logits = logits_out ? logits_out : d->glogits;
-  if (launch_router_gemm(hidden, w_router, logits, T, H, E, d->err, st) != cudaSuccess)
+  if (launch_router_gemm(hidden, w_router, logits_out, d->gscores, d->etab, T, H, E, d->err, st) !=
+      cudaSuccess)
     return MOE_ROUTE_E_CUDA;
   RouteArgs a = {};
-  a.logits = logits;
+  a.logits = d->gscores;
   a.bias = bias;
   a.stab = d->stab;
   a.etab = d->etab;
@@ -220,7 +220,7 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
   a.cnt = local_count;
   a.NE = bins(E, k, local_count);
   a.scale = scale;
-  return launch_route_decode(a, DT_F32, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
+  return launch_route_decode(a, DT_SCORE, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }
 
 int moe_route_device_status(void) {

@@ -26,8 +26,9 @@ cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st);
 cudaError_t launch_empty(int ctas, cudaStream_t st);
 cudaError_t setup_router_gemm();
 int router_gemm_cluster();
-cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float* logits, int T,
-                               int H, int E, int* err, cudaStream_t st);
+cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float* logits,
+                               float* scores, const float2* etab, int T, int H, int E, int* err,
+                               cudaStream_t st);
 cudaError_t setup_prefill_kernels(int* blocks_per_sm);
 cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,
                                  cudaStream_t st);

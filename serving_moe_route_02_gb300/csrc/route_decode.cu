@@ -30,7 +30,7 @@ struct DecodeSmem {
   static constexpr int ROWB = (DT == DT_BF16) ? kE * 2 : kE * 4;
   static constexpr int STAB = (DT == DT_BF16) ? kSigTablePad * 4 : 0;
   static constexpr int o_stab = 0;
-  static constexpr int o_rows = align_up(o_stab + STAB, 128);
+  static constexpr int o_rows = align_up(o_stab + STAB, 128);  // (scores: no table)
   static constexpr int o_ws = align_up(o_rows + kDecodeRowsPerCta * ROWB, 128);
   static constexpr int o_lid = align_up(o_ws + kDecodeRowsPerCta * int(sizeof(WarpScratch)), 128);
   static constexpr int o_counts = align_up(o_lid + kDecodeRowsPerCta * 32 * 4, 128);
@@ -43,6 +43,7 @@ struct DecodeSmem {
 
 static_assert(DecodeSmem<DT_F32>::total <= 227 * 1024, "decode smem (f32) exceeds 227 KB");
 static_assert(DecodeSmem<DT_BF16>::total <= 227 * 1024, "decode smem (bf16) exceeds 227 KB");
+static_assert(DecodeSmem<DT_SCORE>::total <= 227 * 1024, "decode smem (scores) exceeds 227 KB");
 
 template <int DT>
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a) {
@@ -189,6 +190,9 @@ cudaError_t setup_decode_kernels() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        DecodeSmem<DT_F32>::total);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_route_decode<DT_SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           DecodeSmem<DT_SCORE>::total);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(k_route_decode<DT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               DecodeSmem<DT_BF16>::total);
 }
@@ -210,6 +214,10 @@ cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) 
   if (dtype == DT_BF16) {
     cfg.dynamicSmemBytes = DecodeSmem<DT_BF16>::total;
     return cudaLaunchKernelEx(&cfg, k_route_decode<DT_BF16>, a);
+  }
+  if (dtype == DT_SCORE) {
+    cfg.dynamicSmemBytes = DecodeSmem<DT_SCORE>::total;
+    return cudaLaunchKernelEx(&cfg, k_route_decode<DT_SCORE>, a);
   }
   cfg.dynamicSmemBytes = DecodeSmem<DT_F32>::total;
   return cudaLaunchKernelEx(&cfg, k_route_decode<DT_F32>, a);

@@ -42,13 +42,17 @@ struct WarpScratch {
   int32_t slot_id[kMaxK]; // expert id of each slot
 };
 
-enum { DT_F32 = 0, DT_BF16 = 1 };
+// Row input kinds: float32 logits, bfloat16 logits, or float32 scores already equal to
+// sigmoid(logit) (the fused contraction computes them in its epilogue).
+enum { DT_F32 = 0, DT_BF16 = 1, DT_SCORE = 2 };
 
 template <int DT>
 __device__ __forceinline__ float row_sigmoid(const void* row, int e, const float* stab,
                                              const float2* etab) {
   if constexpr (DT == DT_BF16) {
     return sig_bf16(stab, static_cast<const uint16_t*>(row)[e]);
+  } else if constexpr (DT == DT_SCORE) {
+    return static_cast<const float*>(row)[e];
   } else {
     return sig_f32(static_cast<const float*>(row)[e], etab);
   }
@@ -110,7 +114,8 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
       const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float bb = __fadd_rn(sig_f32(x[r], a.etab), bl[4 * q + r]);
+        const float sc = (DT == DT_SCORE) ? x[r] : sig_f32(x[r], a.etab);
+        const float bb = __fadd_rn(sc, bl[4 * q + r]);
         b[4 * q + r] = bb;
         lm2 = fmaxf(lm2, fminf(lm1, bb));
         lm1 = fmaxf(lm1, bb);

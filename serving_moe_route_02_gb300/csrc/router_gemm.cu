@@ -1,6 +1,7 @@
 // router_gemm.cu -- step a0: logits[t][e] = sum_h hidden[t][h] * W[e][h] for decode
 // batches (T <= 64), bf16 operands, fp32 accumulation, on the 5th-generation tensor
-// cores; the routing kernel then runs on the fp32 logits.
+// cores.  The epilogue also applies the score function s = sigmoid(logit), so the
+// routing kernel that follows starts from float32 scores.
 //
 // The router weight (896 x 7168 bf16, 12.85 MB) dominates the traffic: at T <= 64 the
 // contraction does at most ~64 flop per weight byte, so it is bound by reading W once.
@@ -12,9 +13,11 @@
 //   with 2-D TMA loads (128-byte swizzle) into a ring of shared-memory stages, one
 //   thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) into a 128 x N
 //   accumulator in tensor memory, and tcgen05.commit frees each stage;
-//   the 4 warps read the accumulator (tcgen05.ld), stage it in shared memory, and the
-//   cluster reduce-scatters the C partial tiles through distributed shared memory,
-//   summing in a fixed order (deterministic), each CTA writing 128 / C experts.
+//   the 4 warps read the accumulator (tcgen05.ld) into local staging rows, and one
+//   bulk copy per cluster CTA sends it the rows of the experts it owns (distributed
+//   shared memory, completion counted on the owner's mbarrier); each CTA then sums
+//   its 128 / C experts' C partial rows in a fixed order (deterministic) and writes
+//   their logits.
 // All mbarrier waits are bounded; tensor memory is released on every path.
 #include <cuda.h>
 #include <cooperative_groups.h>
@@ -33,10 +36,13 @@ constexpr int kStageH = 64 * kBK * 2;  // room for N <= 64 token rows: 8 KB
 constexpr int kStage = kStageW + kStageH;
 constexpr int kMaxStages = 7;
 constexpr int kTmemCols = 64;
-constexpr int kPartStride = 64 + 1;    // padded row of the staged fp32 partial tile
+constexpr int kRowPad = 64 + 4;       // padded row of 64 token partial sums (conflict-free)
+constexpr int kRecvBytes = kBM * kRowPad * 4;  // receive buffer: C sources x (128/C) rows
 
 struct GemmArgs {
-  float* logits;  // [T, E] fp32 out
+  float* logits;  // [T, E] fp32 logits out, or nullptr
+  float* scores;  // [T, E] fp32 sigmoid(logits) out (read by the routing kernel)
+  const float2* etab;  // 2^(j/64) table of the float32 score function
   int T, Tpad, E;
   int kb_per_cta; // 64-wide K blocks per CTA
   int stages;     // ring depth
@@ -83,6 +89,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+__device__ __forceinline__ uint32_t mapa_cluster(uint32_t local_saddr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
+  return r;
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_router_gemm(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmH,
                   GemmArgs g) {
@@ -93,44 +105,63 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
   const int r = static_cast<int>(cluster.block_rank());
+  const int R = kBM / C;  // experts whose logits this CTA finishes
   const int mtile = blockIdx.x / C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = g.stages;
 
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMaxStages * kStage);
+  float* recv = reinterpret_cast<float*>(smem + kMaxStages * kStage);  // [C][R][kRowPad]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kMaxStages * kStage + kRecvBytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* done = empty + kMaxStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  float* part = reinterpret_cast<float*>(stages);  // reused after the MMAs complete
+  uint64_t* recv_bar = done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
+  float* stage_rows = reinterpret_cast<float*>(stages);  // [128][kRowPad], reuses the ring
+  const int kb0 = r * g.kb_per_cta;
+  const uint32_t stage_bytes = uint32_t(kStageW + g.Tpad * kBK * 2);
+  const uint32_t copy_bytes = uint32_t(R * kRowPad * 4);
 
-  if (warp == 0) {
+  if (threadIdx.x == 0) {
+    // barriers, then every stage's loads at once (the ring holds the whole K slice when
+    // it fits; otherwise the producer loop below refills freed stages)
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    mbar_init(done, 1);
+    mbar_init(recv_bar, 1);
+    fence_mbar_init();
+    for (int kb = 0; kb < NS && kb < g.kb_per_cta; ++kb) {
+      uint8_t* st = stages + kb * kStage;
+      mbar_expect_tx(full + kb, stage_bytes);
+      const int k = (kb0 + kb) * kBK;
+      tma_load_2d(smem_addr(st), &tmW, k, mtile * kBM, smem_addr(full + kb));
+      tma_load_2d(smem_addr(st + kStageW), &tmH, k, 0, smem_addr(full + kb));
+    }
+  }
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (threadIdx.x == 32) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(full + s, 1);
-      mbar_init(empty + s, 1);
-    }
-    mbar_init(done, 1);
-    fence_mbar_init();
-  }
+  // every CTA's barriers exist before any remote copy can reach them; the arrive is
+  // relaxed so that it does not wait for this CTA's TMA loads in flight
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
-  const int kb0 = r * g.kb_per_cta;
-  const uint32_t stage_bytes = uint32_t(kStageW + g.Tpad * kBK * 2);
 
   if (threadIdx.x == 0) {
-    // producer: TMA loads of W and hidden tiles into the ring
-    for (int kb = 0; kb < g.kb_per_cta; ++kb) {
+    mbar_expect_tx(recv_bar, copy_bytes * uint32_t(C));  // C partial blocks will arrive
+    // producer: refill stages freed by the MMAs (only when the K slice exceeds the ring)
+    for (int kb = NS; kb < g.kb_per_cta; ++kb) {
       const int s = kb % NS;
-      if (kb >= NS && !mbar_wait_bounded(empty + s, uint32_t((kb / NS - 1) & 1), g.err)) break;
+      if (!mbar_wait_bounded(empty + s, uint32_t((kb / NS - 1) & 1), g.err)) break;
       uint8_t* st = stages + s * kStage;
       mbar_expect_tx(full + s, stage_bytes);
       const int k = (kb0 + kb) * kBK;
@@ -140,13 +171,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (threadIdx.x == 32) {
     // MMA issuer: 4 MMAs of K = 16 per 64-wide stage
     const uint32_t idesc = mma_idesc(g.Tpad);
-    bool ok = true;
-    for (int kb = 0; kb < g.kb_per_cta && ok; ++kb) {
+    for (int kb = 0; kb < g.kb_per_cta; ++kb) {
       const int s = kb % NS;
-      if (!mbar_wait_bounded(full + s, uint32_t((kb / NS) & 1), g.err)) {
-        ok = false;
-        break;
-      }
+      if (!mbar_wait_bounded(full + s, uint32_t((kb / NS) & 1), g.err)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       uint8_t* st = stages + s * kStage;
       const uint64_t ad = sw128_desc(smem_addr(st));
@@ -160,7 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   __syncwarp();
 
-  // ---- epilogue: accumulator rows -> shared memory
+  // ---- epilogue: accumulator -> local staging rows -> one bulk copy per owner CTA
   const bool acc_ok = mbar_wait_bounded(done, 0, g.err);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   if (acc_ok) {
@@ -185,31 +212,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         : "r"(ta)
         : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    float* prow = part + (warp * 32 + lane) * kPartStride;
+    float4* d4 = reinterpret_cast<float4*>(stage_rows + (warp * 32 + lane) * kRowPad);
 #pragma unroll
-    for (int c = 0; c < 64; ++c) prow[c] = __uint_as_float(v[c]);
+    for (int c = 0; c < 16; ++c)
+      d4[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                          __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
   }
+  fence_proxy_async_smem();  // staging rows visible to the bulk-copy engine
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0)
+  if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
-  cluster.sync();
-
-  // ---- reduce-scatter over the cluster: CTA r sums rows [r R, r R + R) of all C partials
-  const int R = kBM / C;
-  for (int idx = threadIdx.x; idx < R * g.T; idx += kGemmThreads) {
-    const int t = idx / R, i = idx - t * R;
-    const int row = r * R + i;
-    float acc = 0.0f;
-    for (int c = 0; c < C; ++c) {
-      const float* rp = cluster.map_shared_rank(part, c);
-      acc = __fadd_rn(acc, rp[row * kPartStride + t]);
+  if (threadIdx.x == 0) {
+    // rows [o R, o R + R) go to CTA o, into its receive slot for source r
+    for (int o = 0; o < C; ++o) {
+      const uint32_t src = smem_addr(stage_rows + o * R * kRowPad);
+      const uint32_t dst = mapa_cluster(smem_addr(recv + r * R * kRowPad), o);
+      const uint32_t bar = mapa_cluster(smem_addr(recv_bar), o);
+      asm volatile(
+          "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+          "[%3];" ::"r"(dst),
+          "r"(src), "r"(copy_bytes), "r"(bar)
+          : "memory");
     }
-    const int e = mtile * kBM + row;
-    if (e < g.E) g.logits[size_t(t) * g.E + e] = acc;
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
   }
-  cluster.sync();  // keep this CTA's partial tile alive for remote readers
+
+  // ---- this CTA's R experts: sum the C partial rows in source order, float4 stores
+  const bool recv_ok = mbar_wait_bounded(recv_bar, 0, g.err);
+  if (recv_ok) {
+    const int ngrp = R / 4;
+    for (int idx = threadIdx.x; idx < ngrp * g.T; idx += kGemmThreads) {
+      const int t = idx % g.T, i0 = (idx / g.T) * 4;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int c = 0; c < C; ++c) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], recv[(c * R + i0 + q) * kRowPad + t]);
+      }
+      const int e = mtile * kBM + r * R + i0;
+      if (g.logits)
+        *reinterpret_cast<float4*>(g.logits + size_t(t) * g.E + e) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(g.scores + size_t(t) * g.E + e) =
+          make_float4(sig_f32(acc[0], g.etab), sig_f32(acc[1], g.etab), sig_f32(acc[2], g.etab),
+                      sig_f32(acc[3], g.etab));
+    }
+  }
+  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  __syncthreads();
 }
 
 // ------------------------------------------------------------------- host side
@@ -234,8 +285,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
          CUDA_SUCCESS;
 }
 
-constexpr int kGemmSmem = kMaxStages * kStage + 1024 /*align*/ + 256 /*barriers*/;
-static_assert(kMaxStages * kStage >= kBM * kPartStride * 4, "partial tile must fit the ring");
+constexpr int kGemmSmem = kMaxStages * kStage + kRecvBytes + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(kMaxStages * kStage >= kBM * kRowPad * 4, "staged rows must fit the ring");
 static_assert(kGemmSmem <= 227 * 1024, "router contraction smem exceeds 227 KB");
 
 }  // namespace
@@ -279,18 +330,36 @@ cudaError_t setup_router_gemm() {
 
 int router_gemm_cluster() { return g_cluster; }
 
-cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float* logits, int T,
-                               int H, int E, int* err, cudaStream_t st) {
+cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float* logits,
+                               float* scores, const float2* etab, int T, int H, int E, int* err,
+                               cudaStream_t st) {
   const int Tpad = (T + 15) / 16 * 16;
   const int C = g_cluster;
   const int nkb = H / kBK;
   if (Tpad > 64 || nkb % C != 0 || E % kBM != 0) return cudaErrorInvalidValue;
-  CUtensorMap tmW, tmH;
-  if (!make_map(&tmW, w, uint64_t(H), uint64_t(E), kBK, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmH, hidden, uint64_t(H), uint64_t(T), kBK, uint32_t(Tpad)))
-    return cudaErrorInvalidValue;
+  // tensor maps depend only on (pointer, shape): reuse the last ones when unchanged
+  static thread_local CUtensorMap tmW, tmH;
+  static thread_local const void* w_key = nullptr;
+  static thread_local int w_h = 0, w_e = 0;
+  static thread_local const void* h_key = nullptr;
+  static thread_local int h_t = 0, h_h = 0;
+  if (w != w_key || H != w_h || E != w_e) {
+    if (!make_map(&tmW, w, uint64_t(H), uint64_t(E), kBK, kBM)) return cudaErrorInvalidValue;
+    w_key = w;
+    w_h = H;
+    w_e = E;
+  }
+  if (hidden != h_key || T != h_t || H != h_h) {
+    if (!make_map(&tmH, hidden, uint64_t(H), uint64_t(T), kBK, uint32_t(Tpad)))
+      return cudaErrorInvalidValue;
+    h_key = hidden;
+    h_t = T;
+    h_h = H;
+  }
   GemmArgs g = {};
   g.logits = logits;
+  g.scores = scores;
+  g.etab = etab;
   g.T = T;
   g.Tpad = Tpad;
   g.E = E;
