@@ -10,9 +10,10 @@
 // Selection.  tau0 = the k-th largest value of a pool made of the two largest b of
 // every kept lane (a subset of the candidates, so at least k candidates reach tau0).
 // Candidates with b >= tau0 ("survivors", typically 17-22 for k = 16) are compacted
-// one per lane in expert-id order; k rounds of a warp max then pick the slots, the
-// lowest lane (= lowest id) winning exact ties.  If more than 32 survive, a slower
-// exact path extracts the k winners from per-lane maxima.
+// one per lane in expert-id order and sorted by one bitonic network on 32-bit keys
+// (b relative to tau0, then position), so exact ties go to the lower id; when the key
+// range does not allow that, k rounds of a warp maximum pick the slots.  If more than
+// 32 survive, a slower exact path extracts the k winners from per-lane maxima.
 #pragma once
 #include "common.cuh"
 
@@ -35,7 +36,7 @@ struct RouteArgs {
 
 // Per-warp shared scratch of the row routine.
 struct WarpScratch {
-  float b[kE];            // biased scores of the row
+  float b[kEPL * 32];     // biased scores of the kept lanes (kept lane i at [28 i, 28 i + 28))
   float pool[32];         // threshold pool
   uint32_t skey[32];      // survivor keys
   int32_t sid[32];        // survivor expert ids
@@ -79,8 +80,32 @@ struct SlotOut {
   int32_t packed;  // (lid << 16) | bf16 weight bits
 };
 
-// Routes one row.  `row` points to the row's E logits in shared memory (16-byte
-// aligned).  All 32 lanes must call it.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Adds the pair (u, v) to the top-2 list (m1 >= m2); counts equal values with
+// multiplicity.
+__device__ __forceinline__ void top2_pair(float& m1, float& m2, float u, float v) {
+  const float hi = fmaxf(u, v), lo = fminf(u, v);
+  m2 = fmax3(m2, lo, fminf(m1, hi));
+  m1 = fmaxf(m1, hi);
+}
+
+// Bitonic compare-exchange across lanes: keeps the larger value in the lane that the
+// network's direction assigns it to.
+template <typename V>
+__device__ __forceinline__ V bitonic_step(V v, int lane, int size, int stride) {
+  const V o = __shfl_xor_sync(0xffffffffu, v, stride);
+  const bool desc = (lane & size) == 0;
+  const bool lower = (lane & stride) == 0;
+  return (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
+}
+
+// Routes one row.  `row` points to the row's E logits (or scores) in shared memory
+// (16-byte aligned).  All 32 lanes must call it.
 template <int DT>
 __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[kEPL],
                                              const float* stab, const RouteArgs& a,
@@ -89,22 +114,20 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   const int lane = threadIdx.x & 31;
   const int e0 = lane * kEPL;
 
-  // ---- a1, a2: scores, biased scores, lane top-2
+  // ---- a1, a2: scores, biased scores, lane top-2 (two independent lists)
   float b[kEPL];
-  float lm1 = -INFINITY, lm2 = -INFINITY;
+  float xa1 = -INFINITY, xa2 = -INFINITY, xb1 = -INFINITY, xb2 = -INFINITY;
   if constexpr (DT == DT_BF16) {
     const uint2* p = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(row) + e0);
 #pragma unroll
     for (int q = 0; q < kEPL / 4; ++q) {
       const uint2 v = p[q];
-      const uint32_t h[4] = {v.x & 0xFFFFu, v.x >> 16, v.y & 0xFFFFu, v.y >> 16};
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float bb = __fadd_rn(sig_bf16(stab, h[r]), bl[4 * q + r]);
-        b[4 * q + r] = bb;
-        lm2 = fmaxf(lm2, fminf(lm1, bb));
-        lm1 = fmaxf(lm1, bb);
-      }
+      b[4 * q + 0] = __fadd_rn(sig_bf16(stab, v.x & 0xFFFFu), bl[4 * q + 0]);
+      b[4 * q + 1] = __fadd_rn(sig_bf16(stab, v.x >> 16), bl[4 * q + 1]);
+      b[4 * q + 2] = __fadd_rn(sig_bf16(stab, v.y & 0xFFFFu), bl[4 * q + 2]);
+      b[4 * q + 3] = __fadd_rn(sig_bf16(stab, v.y >> 16), bl[4 * q + 3]);
+      top2_pair(xa1, xa2, b[4 * q + 0], b[4 * q + 1]);
+      top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
     }
   } else {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(row) + e0);
@@ -115,19 +138,14 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const float sc = (DT == DT_SCORE) ? x[r] : sig_f32(x[r], a.etab);
-        const float bb = __fadd_rn(sc, bl[4 * q + r]);
-        b[4 * q + r] = bb;
-        lm2 = fmaxf(lm2, fminf(lm1, bb));
-        lm1 = fmaxf(lm1, bb);
+        b[4 * q + r] = __fadd_rn(sc, bl[4 * q + r]);
       }
+      top2_pair(xa1, xa2, b[4 * q + 0], b[4 * q + 1]);
+      top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
     }
   }
-  {
-    float4* d = reinterpret_cast<float4*>(ws.b + e0);
-#pragma unroll
-    for (int q = 0; q < kEPL / 4; ++q)
-      d[q] = make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
-  }
+  const float lm1 = fmaxf(xa1, xb1);
+  const float lm2 = fmax3(fminf(xa1, xb1), xa2, xb2);
 
   // ---- a3: group score = sum of the group's two largest b (4-lane merge of top-2 lists)
   float gm1 = lm1, gm2 = lm2;
@@ -135,9 +153,8 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   for (int o = 1; o < kLanesPerGroup; o <<= 1) {
     const float p1 = __shfl_xor_sync(FULL, gm1, o);
     const float p2 = __shfl_xor_sync(FULL, gm2, o);
-    const float n2 = fmaxf(fminf(gm1, p1), fmaxf(gm2, p2));
+    gm2 = fmax3(fminf(gm1, p1), gm2, p2);
     gm1 = fmaxf(gm1, p1);
-    gm2 = n2;
   }
   const float gs = __fadd_rn(gm1, gm2);
 
@@ -154,7 +171,15 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   const int nk = __popc(kept_lanes);
   const int ki = __popc(kept_lanes & ((1u << lane) - 1u));
 
-  // ---- a5: threshold from the pool of kept lanes' top-2
+  // kept lanes park their biased scores for the survivor extraction below
+  if (kept) {
+    float4* d = reinterpret_cast<float4*>(ws.b + ki * kEPL);
+#pragma unroll
+    for (int q = 0; q < kEPL / 4; ++q)
+      d[q] = make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+  }
+
+  // ---- a5: threshold tau0 = k-th largest of the pool of kept lanes' top-2
   ws.pool[lane] = -INFINITY;
   __syncwarp();
   int pool_n;
@@ -175,18 +200,31 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   float tau0 = -INFINITY;
   if (pool_n >= a.k) {
     float v = ws.pool[lane];
-    // bitonic sort, descending across lanes
+    if (a.k <= 16) {
+      // sort each half of 16 in opposite directions, keep the larger of each pair:
+      // lanes 0..15 then hold the pool's 16 largest values
 #pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
+      for (int size = 2; size <= 16; size <<= 1)
 #pragma unroll
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        const float o = __shfl_xor_sync(FULL, v, stride);
-        const bool desc = (lane & size) == 0;
-        const bool lower = (lane & stride) == 0;
-        v = (lower == desc) ? fmaxf(v, o) : fminf(v, o);
+        for (int stride = size >> 1; stride > 0; stride >>= 1) v = bitonic_step(v, lane, size, stride);
+      v = fmaxf(v, __shfl_xor_sync(FULL, v, 16));
+      if (a.k == 16) {
+        float mn = v;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
+        tau0 = __shfl_sync(FULL, mn, 0);
+      } else {
+#pragma unroll
+        for (int stride = 8; stride > 0; stride >>= 1) v = bitonic_step(v, lane & 15, 32, stride);
+        tau0 = __shfl_sync(FULL, v, a.k - 1);
       }
+    } else {
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) v = bitonic_step(v, lane, size, stride);
+      tau0 = __shfl_sync(FULL, v, a.k - 1);
     }
-    tau0 = __shfl_sync(FULL, v, a.k - 1);
   }
 
   uint32_t smask = 0;
@@ -204,24 +242,49 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   const int total = __shfl_sync(FULL, incl, 31);
   __syncwarp();  // ws.b visible to the warp
 
+  // composite 32-bit keys (b, position) need tau0 > 0 and survivors within 2^26 float
+  // steps of it; otherwise order keys and k rounds of a warp maximum
+  const bool fast = total <= 32 && tau0 > 0.0f;
+  uint32_t bmax_all = 0;
+  if (fast) {
+    float m = kept ? lm1 : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    bmax_all = __float_as_uint(m);
+  }
+  const bool keys32 = fast && (bmax_all - __float_as_uint(tau0)) < (1u << 26);
+
   if (total <= 32) {
     int pos = incl - c;
     while (smask) {
       const int i = __ffs(smask) - 1;
       smask &= smask - 1u;
-      ws.skey[pos] = fkey(ws.b[e0 + i]);
+      const float bv = ws.b[ki * kEPL + i];
+      ws.skey[pos] = keys32 ? (((__float_as_uint(bv) - __float_as_uint(tau0) + 1u) << 5) |
+                               uint32_t(31 - pos))
+                            : fkey(bv);
       ws.sid[pos] = e0 + i;
       ++pos;
     }
     __syncwarp();
-    uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
-    const int my_id = (lane < total) ? ws.sid[lane] : 0;
-    for (int j = 0; j < a.k; ++j) {
-      const uint32_t top = __reduce_max_sync(FULL, key);
-      const int win = __ffs(__ballot_sync(FULL, key == top)) - 1;
-      if (lane == win) {
-        ws.slot_id[j] = my_id;
-        key = 0u;
+    if (keys32) {
+      // one bitonic sort of (b, position) keys: slot j = lane j after the sort
+      uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) key = bitonic_step(key, lane, size, stride);
+      if (lane < a.k) ws.slot_id[lane] = ws.sid[31 - int(key & 31u)];
+    } else {
+      uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
+      const int my_id = (lane < total) ? ws.sid[lane] : 0;
+      for (int j = 0; j < a.k; ++j) {
+        const uint32_t top = __reduce_max_sync(FULL, key);
+        const int win = __ffs(__ballot_sync(FULL, key == top)) - 1;
+        if (lane == win) {
+          ws.slot_id[j] = my_id;
+          key = 0u;
+        }
       }
     }
   } else {
@@ -233,7 +296,7 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
       if (!kept) return;
       for (int i = 0; i < kEPL; ++i) {
         if (taken & (1u << i)) continue;
-        const uint32_t kk = fkey(ws.b[e0 + i]);
+        const uint32_t kk = fkey(ws.b[ki * kEPL + i]);
         if (kk > bk) {
           bk = kk;
           bi = i;
