@@ -161,5 +161,16 @@ def cfg4(T: int = 4096, E: int = E_KIMI, off: int = 0, cnt: int = 0, dtype: str 
     return out
 
 
+def cfg_bf16_patterns(T: int, E: int = E_KIMI, off: int = 0, cnt: int = 0, seed: int = 9) -> dict:
+    """bf16 logits drawn uniformly over bit patterns (seed 9), non-finite patterns made
+    finite by clearing the top exponent bit: zeros, subnormals, magnitudes far below and
+    far above the range where the score varies, both signs."""
+    h = (raw64(seed, T * E) >> np.uint64(48)).astype(np.uint16)
+    inf_nan = (h & np.uint16(0x7F80)) == np.uint16(0x7F80)
+    h[inf_nan] ^= np.uint16(0x4000)
+    return dict(logits=h.reshape(T, E), dtype="bf16", bias=bias_standard(E), T=T, E=E, k=K_KIMI,
+                G=G_KIMI, Kg=KG_KIMI, scale=SCALE_KIMI, off=off, cnt=cnt)
+
+
 def num_local_experts(E: int, ep: int) -> int:
     return E // ep

@@ -174,6 +174,7 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
       const int grid_cap = d->pw.grid_max;
       int grid = (T + 15) / 16;
       if (grid > grid_cap) grid = grid_cap;
+      if (!prefill_fits(T, grid)) return MOE_ROUTE_E_UNSUPPORTED;
       ce = launch_route_prefill(a, dt, d->pw, grid, st);
     }
   }

@@ -30,6 +30,9 @@ cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float*
                                float* scores, const float2* etab, int T, int H, int E, int* err,
                                cudaStream_t st);
 cudaError_t setup_prefill_kernels(int* blocks_per_sm);
+// False when a warp of the persistent kernel would get 65,536 rows or more (its 16-bit
+// bin counters would overflow); the launcher then refuses the launch.
+bool prefill_fits(int T, int grid);
 cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,
                                  cudaStream_t st);
 

@@ -5,12 +5,15 @@
 // warps per 8 rows, up to 8 CTAs in one cluster.  Each warp routes one row (the
 // prior art on the pages, FlashInfer's routingIndicesClusterKernel for
 // Tier<896, 16>, also ran decode routing as one cluster -- sglang PR #37).  The
-// histogram, scan and stable permutation need every row's ids: after a cluster
-// barrier each CTA reads all CTAs' relabelled ids through distributed shared memory,
-// builds the histogram and a per-id bitmask of the rows containing it (ids are unique
-// within a row, so the stable rank of (t, j) is the number of earlier rows holding the
-// same id), scans, and writes the permutation entries of its own rows.  No global
-// workspace, no atomics in global memory, no spin waits.
+// histogram, scan and stable permutation need every row's ids.  After routing, each
+// warp stores its row's relabelled ids into an id array in every CTA of the cluster
+// (vector stores through distributed shared memory); after one cluster barrier every
+// CTA holds all rows' ids and builds, in its own shared memory, a mask of the rows
+// holding each id (two 32-bit words per id).  Counts are the masks' popcounts, a block
+// scan gives offsets, and since ids are unique within a row the stable rank of (t, j)
+// is the number of earlier rows in its id's mask.  Each CTA writes the permutation
+// entries of its own rows.  No global workspace, no atomics in global memory, no spin
+// waits.
 #include <cooperative_groups.h>
 
 #include "launch.h"
@@ -33,8 +36,7 @@ struct DecodeSmem {
   static constexpr int o_rows = align_up(o_stab + STAB, 128);  // (scores: no table)
   static constexpr int o_ws = align_up(o_rows + kDecodeRowsPerCta * ROWB, 128);
   static constexpr int o_lid = align_up(o_ws + kDecodeRowsPerCta * int(sizeof(WarpScratch)), 128);
-  static constexpr int o_counts = align_up(o_lid + kDecodeRowsPerCta * 32 * 4, 128);
-  static constexpr int o_offs = align_up(o_counts + kMaxBins * 4, 128);
+  static constexpr int o_offs = align_up(o_lid + 64 * kMaxK * 4, 128);  // lid: [64 rows][32]
   static constexpr int o_mask = align_up(o_offs + (kMaxBins + 1) * 4, 128);
   static constexpr int o_tmp = align_up(o_mask + kMaxBins * 8, 128);
   static constexpr int o_mbar = align_up(o_tmp + 32 * 4, 128);
@@ -44,8 +46,39 @@ struct DecodeSmem {
 static_assert(DecodeSmem<DT_F32>::total <= 227 * 1024, "decode smem (f32) exceeds 227 KB");
 static_assert(DecodeSmem<DT_BF16>::total <= 227 * 1024, "decode smem (bf16) exceeds 227 KB");
 static_assert(DecodeSmem<DT_SCORE>::total <= 227 * 1024, "decode smem (scores) exceeds 227 KB");
+static_assert(kDecodeRowsPerCta * kDecodeMaxCtas <= 64, "row masks are 64 bits");
 
-template <int DT>
+// Exclusive scan over the bins of counts popc(mask[e]) into offs[0..n], offs[n] = total;
+// two block barriers.  mask[e] holds rows 0..31 in its low word, 32..63 in its high word.
+__device__ __forceinline__ void mask_count_scan(const unsigned long long* mask, int* offs, int n,
+                                                int* tmp) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, wid = tid >> 5;
+  const int per = (n + nt - 1) / nt;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += __popcll(mask[i]);
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) tmp[wid] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int i = 0; i < wid; ++i) run += tmp[i];
+  for (int i = lo; i < hi; ++i) {
+    offs[i] = run;
+    run += __popcll(mask[i]);
+  }
+  if (hi == n && lo < hi) offs[n] = run;
+  if (n == 0 && tid == 0) offs[0] = 0;
+  __syncthreads();
+}
+
+// SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).
+template <int DT, bool SPEC>
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a) {
   using L = DecodeSmem<DT>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -53,15 +86,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   float* stab = reinterpret_cast<float*>(smem + L::o_stab);
   uint8_t* rows = smem + L::o_rows;
   WarpScratch* wsp = reinterpret_cast<WarpScratch*>(smem + L::o_ws);
-  int32_t* lid_s = reinterpret_cast<int32_t*>(smem + L::o_lid);
-  int* counts_s = reinterpret_cast<int*>(smem + L::o_counts);
   int* offs_s = reinterpret_cast<int*>(smem + L::o_offs);
   unsigned long long* mask_s = reinterpret_cast<unsigned long long*>(smem + L::o_mask);
   int* tmp = reinterpret_cast<int*>(smem + L::o_tmp);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::o_mbar);
 
+  int32_t* lid_all = reinterpret_cast<int32_t*>(smem + L::o_lid);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int crank = static_cast<int>(cluster.block_rank());
+  const int nctas = static_cast<int>(cluster.num_blocks());
   const int row0 = crank * kDecodeRowsPerCta;
   const int nrows = max(0, min(kDecodeRowsPerCta, a.T - row0));
   const uint32_t bytes = uint32_t(nrows) * L::ROWB + uint32_t(L::STAB);
@@ -78,52 +111,67 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
              uint32_t(nrows) * L::ROWB, mbar);
   }
+  // every CTA of the cluster must be running before another one stores into its shared
+  // memory: arrive now (relaxed: nothing to publish, and no wait for the copies in
+  // flight), wait after routing
+  for (int e = tid; e < a.NE; e += kDecodeThreads) mask_s[e] = 0ull;
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   float bl[kEPL];
   load_lane_bias(a.bias, bl);
   if (have) mbar_wait_bounded(mbar, 0, a.err);
 
+  SlotOut o = {};
   if (w < nrows) {
-    const SlotOut o = route_row<DT>(rows + w * L::ROWB, bl, stab, a, wsp[w]);
+    o = route_row<DT, SPEC ? 16 : 0, SPEC ? 4 : 0>(rows + w * L::ROWB, bl, stab, a, wsp[w]);
     const int t = row0 + w;
     if (lane < a.k) {
       a.packed[size_t(t) * a.k + lane] = o.packed;
       if (a.ids) a.ids[size_t(t) * a.k + lane] = o.id;
-      lid_s[w * 32 + lane] = o.lid;
+      lid_all[t * kMaxK + lane] = o.lid;
     }
   }
-  cluster.sync();
-
-  // ---- a9..a11 over all rows of the cluster
-  for (int e = tid; e < a.NE; e += kDecodeThreads) {
-    counts_s[e] = 0;
-    mask_s[e] = 0ull;
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  // ---- a9..a11: this warp's row of ids goes to every other CTA, 16 bytes per store
+  if (w < nrows) {
+    __syncwarp();
+    const int t = row0 + w;
+    const int nch = (a.k + 3) / 4;
+    const uint32_t src = smem_addr(lid_all + t * kMaxK);
+    for (int p = lane; p < nctas * nch; p += 32) {
+      const int c = p / nch, q = p - c * nch;
+      if (c == crank) continue;
+      uint4 v;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(src + 16u * q));
+      uint32_t dst;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(src + 16u * q), "r"(c));
+      asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x),
+                   "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
   }
-  __syncthreads();
-  const int ntot = a.T * a.k;
-  for (int x = tid; x < ntot; x += kDecodeThreads) {
+  cluster.sync();  // release the stores above, acquire every other CTA's
+  uint32_t* mask32 = reinterpret_cast<uint32_t*>(mask_s);
+  for (int x = tid; x < a.T * a.k; x += kDecodeThreads) {
     const int t = x / a.k, j = x - t * a.k;
-    const int32_t* rl = cluster.map_shared_rank(lid_s, t / kDecodeRowsPerCta);
-    const int l = rl[(t % kDecodeRowsPerCta) * 32 + j];
-    atomicAdd(&counts_s[l], 1);
-    atomicOr(&mask_s[l], 1ull << t);
+    atomicOr(mask32 + 2 * lid_all[t * kMaxK + j] + (t >> 5), 1u << (t & 31));
   }
   __syncthreads();
-  block_exclusive_scan(counts_s, offs_s, a.NE, tmp);
+
+  mask_count_scan(mask_s, offs_s, a.NE, tmp);
   if (crank == 0) {
     for (int e = tid; e < a.NE; e += kDecodeThreads) {
-      a.counts[e] = counts_s[e];
+      a.counts[e] = __popcll(mask_s[e]);
       a.offsets[e] = offs_s[e];
     }
     if (tid == 0) a.offsets[a.NE] = offs_s[a.NE];
   }
-  for (int x = tid; x < nrows * a.k; x += kDecodeThreads) {
-    const int ww = x / a.k, j = x - ww * a.k;
-    const int t = row0 + ww;
-    const int l = lid_s[ww * 32 + j];
-    const int pos = offs_s[l] + __popcll(mask_s[l] & ((1ull << t) - 1ull));
-    a.perm[pos] = t * a.k + j;
+  if (w < nrows && lane < a.k) {
+    const int t = row0 + w;
+    const int pos = offs_s[o.lid] + __popcll(mask_s[o.lid] & ((1ull << t) - 1ull));
+    a.perm[pos] = t * a.k + lane;
   }
-  cluster.sync();  // keep this CTA's shared memory alive for remote readers
 }
 
 // --------------------------------------------------------------- sigmoid table
@@ -185,16 +233,26 @@ cudaError_t launch_empty(int ctas, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, k_empty);
 }
 
+template <int DT, bool SPEC>
+static cudaError_t set_decode_smem() {
+  return cudaFuncSetAttribute(k_route_decode<DT, SPEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              DecodeSmem<DT>::total);
+}
+
 cudaError_t setup_decode_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(k_route_decode<DT_F32>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       DecodeSmem<DT_F32>::total);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_route_decode<DT_SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           DecodeSmem<DT_SCORE>::total);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_route_decode<DT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DecodeSmem<DT_BF16>::total);
+  cudaError_t e;
+  if ((e = set_decode_smem<DT_F32, false>()) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_F32, true>()) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_BF16, false>()) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_BF16, true>()) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_SCORE, false>()) != cudaSuccess) return e;
+  return set_decode_smem<DT_SCORE, true>();
+}
+
+template <int DT, bool SPEC>
+static cudaError_t launch_decode_t(cudaLaunchConfig_t& cfg, const RouteArgs& a) {
+  cfg.dynamicSmemBytes = DecodeSmem<DT>::total;
+  return cudaLaunchKernelEx(&cfg, k_route_decode<DT, SPEC>, a);
 }
 
 cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) {
@@ -211,16 +269,10 @@ cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (dtype == DT_BF16) {
-    cfg.dynamicSmemBytes = DecodeSmem<DT_BF16>::total;
-    return cudaLaunchKernelEx(&cfg, k_route_decode<DT_BF16>, a);
-  }
-  if (dtype == DT_SCORE) {
-    cfg.dynamicSmemBytes = DecodeSmem<DT_SCORE>::total;
-    return cudaLaunchKernelEx(&cfg, k_route_decode<DT_SCORE>, a);
-  }
-  cfg.dynamicSmemBytes = DecodeSmem<DT_F32>::total;
-  return cudaLaunchKernelEx(&cfg, k_route_decode<DT_F32>, a);
+  const bool spec = a.k == 16 && a.Kg == 4;
+  if (dtype == DT_BF16) return spec ? launch_decode_t<DT_BF16, true>(cfg, a) : launch_decode_t<DT_BF16, false>(cfg, a);
+  if (dtype == DT_SCORE) return spec ? launch_decode_t<DT_SCORE, true>(cfg, a) : launch_decode_t<DT_SCORE, false>(cfg, a);
+  return spec ? launch_decode_t<DT_F32, true>(cfg, a) : launch_decode_t<DT_F32, false>(cfg, a);
 }
 
 }  // namespace moe

@@ -146,5 +146,6 @@ extern "C" int moe_route_noalloc(const void* logits, int logits_dtype, const flo
   ws.grid_max = kNoallocMaxCtas;
   int grid = (T + 15) / 16;
   if (grid > d.grid_max) grid = d.grid_max;
+  if (!prefill_fits(T, grid)) return MOE_ROUTE_E_UNSUPPORTED;
   return launch_route_prefill(a, dt, ws, grid, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }

@@ -1,17 +1,23 @@
 // route_prefill.cu -- prefill-size routing (thousands of rows) in one persistent,
-// cooperative launch: one CTA of 16 warps per SM, contiguous row ranges per CTA.
+// cooperative launch: one CTA of 16 warps per SM, a contiguous row range per CTA and a
+// contiguous sub-range per warp.
 //
 // Phase 1 (the streaming part, bound by HBM and issue rate): every warp is its own row
 //   engine.  Its lane 0 keeps D rows in flight with one-dimensional bulk copies
 //   (cp.async.bulk, completion on a per-slot mbarrier) into a private ring in shared
 //   memory; the warp routes each row (route_row), writes packed ids coalesced, and
-//   counts the relabelled ids into the CTA's shared-memory histogram.
-// Grid barrier 1, then a column scan: for each expert bin e, one warp scans the
-//   per-CTA counts hist[e][0..grid) into prefix[e][c] and total counts[e].
-// Grid barrier 2, then phase 3: every CTA scans counts into offsets (CTA 0 writes
-//   counts and offsets), and walks its own rows in order, 32 rows at a time: a
-//   per-bin 32-bit mask of the rows holding that bin gives each entry's stable rank,
-//   so perm[offsets[e] + prefix[e][c] + rank] = t * k + j.
+//   counts the relabelled ids in its own 16-bit counters wcnt[w][bin].
+// Column pass: per bin, the 16 warp counters become 32-bit exclusive prefixes over
+//   warps (written over the ring, free by then) and their sum is the CTA's count,
+//   written to the expert-major matrix hist[bin][cta].
+// Grid barrier 1, then a column scan: for each bin one warp turns hist[bin][0..grid)
+//   into exclusive prefixes over CTAs and the bin's total.
+// Grid barrier 2, then phase 3: every CTA scans the totals into offsets (CTA 0 writes
+//   counts and offsets), adds its own CTA prefix, and every warp walks its rows in
+//   order: the entry (t, j) with relabelled id l goes to
+//   perm[offsets[l] + cta prefix + warp prefix + running count of l in this warp],
+//   which is its stable (id, token, slot) position, since ids are unique in a row.
+//   No block barrier inside the walk.
 // Every wait (mbarrier, grid barrier) is bounded in time; a wait that runs out sets
 // the device status word and the kernel returns.
 #include <cooperative_groups.h>
@@ -22,7 +28,6 @@ namespace moe {
 
 constexpr int kPrefillWarps = 16;
 constexpr int kPrefillThreads = 32 * kPrefillWarps;
-constexpr int kChunkRows = 32;
 
 __host__ __device__ constexpr int p_align(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -34,43 +39,42 @@ struct PrefillSmem {
   static constexpr int o_stab = 0;
   static constexpr int o_ring = p_align(o_stab + STAB, 128);
   static constexpr int o_ws = p_align(o_ring + kPrefillWarps * D * ROWB, 128);
-  static constexpr int o_hist = p_align(o_ws + kPrefillWarps * int(sizeof(WarpScratch)), 128);
+  static constexpr int o_wcnt = p_align(o_ws + kPrefillWarps * int(sizeof(WarpScratch)), 128);
+  static constexpr int o_hist = p_align(o_wcnt + kPrefillWarps * kMaxBins * 2, 128);
   static constexpr int o_base = p_align(o_hist + (kMaxBins + 1) * 4, 128);
-  static constexpr int o_mask = p_align(o_base + (kMaxBins + 1) * 4, 128);
-  static constexpr int o_tmp = p_align(o_mask + kMaxBins * 4, 128);
+  static constexpr int o_tmp = p_align(o_base + (kMaxBins + 1) * 4, 128);
   static constexpr int o_mbar = p_align(o_tmp + 33 * 4, 128);
   static constexpr int total = o_mbar + kPrefillWarps * D * 8 + 64;
 };
 
 static_assert(PrefillSmem<DT_F32>::total <= 227 * 1024, "prefill smem (f32) exceeds 227 KB");
 static_assert(PrefillSmem<DT_BF16>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
+static_assert(kMaxBins % 2 == 0, "16-bit counters are updated in 32-bit pairs");
+static_assert(PrefillSmem<DT_BF16>::D * PrefillSmem<DT_BF16>::ROWB >= kMaxBins * 4 &&
+                  PrefillSmem<DT_F32>::D * PrefillSmem<DT_F32>::ROWB >= kMaxBins * 4,
+              "32-bit warp prefixes reuse the ring");
 
-// Grid-wide barrier for a cooperative launch; bounded in time.  bar[0] counts
-// arrivals, bar[1] is the generation.  Returns false if the wait ran out.
+// Grid-wide barrier for a cooperative launch, bounded in time.  One arrival counter:
+// CTA 0 adds 2^31 - (nblocks - 1), every other CTA adds 1, so the counter's top bit
+// flips exactly when all have arrived (it starts at 0 and every completed barrier
+// leaves it at 0 or 2^31).  Returns false if the wait ran out.
 __device__ bool grid_barrier(unsigned* bar, unsigned nblocks, int* err, int* flag_s) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned gen0;
-    asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(gen0) : "l"(bar + 1) : "memory");
+    const unsigned add = (blockIdx.x == 0) ? 0x80000000u - (nblocks - 1u) : 1u;
+    unsigned old;
     __threadfence();
-    const unsigned prev = atomicAdd(bar, 1u);
+    asm volatile("atom.release.gpu.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(bar), "r"(add) : "memory");
     int ok = 1;
-    if (prev == nblocks - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      for (;;) {
-        unsigned g;
-        asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(g) : "l"(bar + 1) : "memory");
-        if (g != gen0) break;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          atomicExch(err, kErrTimeout);
-          ok = 0;
-          break;
-        }
-        __nanosleep(64);
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      unsigned cur;
+      asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(cur) : "l"(bar) : "memory");
+      if ((cur ^ old) & 0x80000000u) break;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicExch(err, kErrTimeout);
+        ok = 0;
+        break;
       }
     }
     __threadfence();
@@ -80,7 +84,50 @@ __device__ bool grid_barrier(unsigned* bar, unsigned nblocks, int* err, int* fla
   return *flag_s != 0;
 }
 
-template <int DT>
+// Exclusive scan of in[0..n) into out[0..n], out[n] = total, with two block barriers.
+// All threads of the block call it; `tmp` holds at least 32 ints.  in and out may alias.
+__device__ __forceinline__ void block_scan_fast(const int* in, int* out, int n, int* tmp) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, wid = tid >> 5;
+  const int per = (n + nt - 1) / nt;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+  int v[4];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[i] = (lo + i < hi) ? in[lo + i] : 0;
+    sum += v[i];
+  }
+  for (int i = lo + 4; i < hi; ++i) sum += in[i];  // only when n > 4 * blockDim.x
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) tmp[wid] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int i = 0; i < wid; ++i) run += tmp[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (lo + i < hi) {
+      out[lo + i] = run;
+      run += v[i];
+    }
+  }
+  for (int i = lo + 4; i < hi; ++i) {
+    const int u = in[i];
+    out[i] = run;
+    run += u;
+  }
+  if (hi == n && lo < hi) out[n] = run;
+  if (n == 0 && tid == 0) out[0] = 0;
+  __syncthreads();
+}
+
+// SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).
+template <int DT, bool SPEC>
 __global__ void __launch_bounds__(kPrefillThreads, 1)
     k_route_prefill(RouteArgs a, PrefillWS pw) {
   using L = PrefillSmem<DT>;
@@ -88,9 +135,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   float* stab = reinterpret_cast<float*>(smem + L::o_stab);
   uint8_t* ring_all = smem + L::o_ring;
   WarpScratch* wsp = reinterpret_cast<WarpScratch*>(smem + L::o_ws);
+  uint16_t* wcnt_all = reinterpret_cast<uint16_t*>(smem + L::o_wcnt);
   int* hist_s = reinterpret_cast<int*>(smem + L::o_hist);
   int* base_s = reinterpret_cast<int*>(smem + L::o_base);
-  unsigned* mask_s = reinterpret_cast<unsigned*>(smem + L::o_mask);
   int* tmp = reinterpret_cast<int*>(smem + L::o_tmp);
   uint64_t* mbar_all = reinterpret_cast<uint64_t*>(smem + L::o_mbar);
 
@@ -98,12 +145,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int grid = gridDim.x, cta = blockIdx.x;
   const int r0 = int((long long)a.T * cta / grid);
   const int r1 = int((long long)a.T * (cta + 1) / grid);
-  const int nw = (r1 - r0 > w) ? (r1 - r0 - w + kPrefillWarps - 1) / kPrefillWarps : 0;
+  // this warp's rows: [wr0, wr1)
+  const int per_warp = (r1 - r0 + kPrefillWarps - 1) / kPrefillWarps;
+  const int wr0 = min(r1, r0 + w * per_warp);
+  const int wr1 = min(r1, wr0 + per_warp);
+  const int nw = wr1 - wr0;
   uint8_t* ring = ring_all + w * L::D * L::ROWB;
   uint64_t* mb = mbar_all + w * L::D;
+  uint16_t* wcnt = wcnt_all + w * kMaxBins;
+  uint32_t* wcnt32 = reinterpret_cast<uint32_t*>(wcnt);
   const uint8_t* logits = static_cast<const uint8_t*>(a.logits);
 
-  // ---- setup: mbarriers, sigmoid table, first rows in flight
+  // ---- setup: mbarriers, counters, sigmoid table, first rows in flight
   if (lane == 0) {
     for (int d = 0; d < L::D; ++d) mbar_init(mb + d, 1);
     fence_mbar_init();
@@ -113,7 +166,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     mbar_init(tab_bar, 1);
     fence_mbar_init();
   }
-  for (int e = tid; e < a.NE; e += kPrefillThreads) hist_s[e] = 0;
+  for (int e = lane; e < (a.NE + 1) / 2; e += 32) wcnt32[e] = 0u;
   __syncthreads();
   if (tid == 0 && L::STAB) {
     mbar_expect_tx(tab_bar, L::STAB);
@@ -121,9 +174,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   }
   if (lane == 0) {
     for (int d = 0; d < L::D && d < nw; ++d) {
-      const int t = r0 + w + d * kPrefillWarps;
       mbar_expect_tx(mb + d, L::ROWB);
-      bulk_g2s(ring + d * L::ROWB, logits + size_t(t) * L::ROWB, L::ROWB, mb + d);
+      bulk_g2s(ring + d * L::ROWB, logits + size_t(wr0 + d) * L::ROWB, L::ROWB, mb + d);
     }
   }
   float bl[kEPL];
@@ -135,42 +187,70 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     const int slot = i % L::D;
     const uint32_t par = uint32_t(i / L::D) & 1u;
     mbar_wait_bounded(mb + slot, par, a.err);
-    const int t = r0 + w + i * kPrefillWarps;
-    const SlotOut o = route_row<DT>(ring + slot * L::ROWB, bl, stab, a, wsp[w]);
+    const int t = wr0 + i;
+    const SlotOut o =
+        route_row<DT, SPEC ? 16 : 0, SPEC ? 4 : 0>(ring + slot * L::ROWB, bl, stab, a, wsp[w]);
     if (lane < a.k) {
       a.packed[size_t(t) * a.k + lane] = o.packed;
       if (a.ids) a.ids[size_t(t) * a.k + lane] = o.id;
-      atomicAdd(&hist_s[o.lid], 1);
+      // ids are unique in a row; two lanes may share a 32-bit word (bins 2m, 2m+1)
+      atomicAdd(&wcnt32[o.lid >> 1], 1u << ((o.lid & 1) * 16));
     }
     __syncwarp();
     if (lane == 0 && i + L::D < nw) {
       fence_proxy_async_smem();
       mbar_expect_tx(mb + slot, L::ROWB);
-      bulk_g2s(ring + slot * L::ROWB, logits + size_t(t + L::D * kPrefillWarps) * L::ROWB,
-               L::ROWB, mb + slot);
+      bulk_g2s(ring + slot * L::ROWB, logits + size_t(t + L::D) * L::ROWB, L::ROWB, mb + slot);
     }
   }
   __syncthreads();
-  for (int e = tid; e < a.NE; e += kPrefillThreads) pw.hist[size_t(e) * pw.grid_max + cta] = hist_s[e];
+
+  // ---- column pass: warp prefixes per bin (32-bit, over the ring: every bulk copy into
+  //      it has completed), CTA count per bin
+  int* wpre_all = reinterpret_cast<int*>(ring_all);
+  for (int e = tid; e < a.NE; e += kPrefillThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kPrefillWarps; ++w2) {
+      const int v = wcnt_all[w2 * kMaxBins + e];
+      wpre_all[w2 * kMaxBins + e] = run;
+      run += v;
+    }
+    pw.hist[size_t(e) * pw.grid_max + cta] = run;
+  }
 
   int* flag_s = tmp + 32;
   if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
 
-  // ---- column scan over CTAs, one warp per expert bin
+  // ---- column scan over CTAs, one warp per bin; lane l covers up to 8 consecutive CTAs
+  //      per pass of 256
   for (int e = cta * kPrefillWarps + w; e < a.NE; e += grid * kPrefillWarps) {
     const int* h = pw.hist + size_t(e) * pw.grid_max;
     int* p = pw.prefix + size_t(e) * pw.grid_max;
     int carry = 0;
-    for (int c0 = 0; c0 < grid; c0 += 32) {
-      const int c = c0 + lane;
-      const int v = (c < grid) ? h[c] : 0;
-      int incl = v;
+    for (int c0 = 0; c0 < grid; c0 += 256) {
+      const int span = min(256, grid - c0);
+      const int per = (span + 31) / 32;
+      const int cl = c0 + lane * per;
+      int v[8];
+      int sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        v[i] = (i < per && cl + i < c0 + span) ? __ldcg(h + cl + i) : 0;
+        sum += v[i];
+      }
+      int incl = sum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += n;
       }
-      if (c < grid) p[c] = carry + incl - v;
+      int run = carry + incl - sum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i < per && cl + i < c0 + span) p[cl + i] = run;
+        run += v[i];
+      }
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) pw.counts[e] = carry;
@@ -179,9 +259,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
 
   // ---- phase 3: offsets, then this CTA's permutation entries
-  for (int e = tid; e < a.NE; e += kPrefillThreads) hist_s[e] = pw.counts[e];
+  for (int e = tid; e < a.NE; e += kPrefillThreads) hist_s[e] = __ldcg(pw.counts + e);
   __syncthreads();
-  block_exclusive_scan(hist_s, base_s, a.NE, tmp);
+  block_scan_fast(hist_s, base_s, a.NE, tmp);
   if (cta == 0) {
     for (int e = tid; e < a.NE; e += kPrefillThreads) {
       a.counts[e] = hist_s[e];
@@ -189,61 +269,68 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
     if (tid == 0) a.offsets[a.NE] = base_s[a.NE];
   }
+  for (int e = tid; e < a.NE; e += kPrefillThreads) base_s[e] += __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
   __syncthreads();
-  for (int e = tid; e < a.NE; e += kPrefillThreads) {
-    base_s[e] += pw.prefix[size_t(e) * pw.grid_max + cta];
-    mask_s[e] = 0u;
-  }
-  __syncthreads();
-  for (int cr = r0; cr < r1; cr += kChunkRows) {
-    const int nr = min(kChunkRows, r1 - cr);
-    const int ne = nr * a.k;
-    const int32_t* pk = a.packed + size_t(cr) * a.k;
-    for (int x = tid; x < ne; x += kPrefillThreads) {
-      const int rr = x / a.k;
-      const int l = int(uint32_t(pk[x]) >> 16);
-      atomicOr(&mask_s[l], 1u << rr);
-    }
-    __syncthreads();
-    for (int x = tid; x < ne; x += kPrefillThreads) {
-      const int rr = x / a.k, j = x - rr * a.k;
-      const int l = int(uint32_t(pk[x]) >> 16);
-      const int pos = base_s[l] + __popc(mask_s[l] & ((1u << rr) - 1u));
-      a.perm[pos] = (cr + rr) * a.k + j;
-    }
-    __syncthreads();
-    for (int e = tid; e < a.NE; e += kPrefillThreads) {
-      const unsigned m = mask_s[e];
-      if (m) {
-        base_s[e] += __popc(m);
-        mask_s[e] = 0u;
+  if (lane < a.k) {
+    // rows in order; packed ids are loaded eight rows ahead of their use
+    int* wpre = wpre_all + w * kMaxBins;
+    const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
+    constexpr int kAhead = 8;
+    int32_t x[kAhead];
+#pragma unroll
+    for (int q = 0; q < kAhead; ++q) x[q] = (q < nw) ? a.packed[size_t(wr0 + q) * a.k + lane] : 0;
+    for (int i0 = 0; i0 < nw; i0 += kAhead) {
+#pragma unroll
+      for (int q = 0; q < kAhead; ++q) {
+        const int i = i0 + q;
+        if (i < nw) {
+          const int l = int(uint32_t(x[q]) >> 16);
+          const int r = wpre[l];
+          wpre[l] = r + 1;
+          a.perm[base_s[l] + r] = (wr0 + i) * a.k + lane;
+          x[q] = (i + kAhead < nw) ? a.packed[size_t(wr0 + i + kAhead) * a.k + lane] : 0;
+        }
+        __syncwarp(kmask);  // the next row may count the same bin in another lane
       }
     }
-    __syncthreads();
   }
 }
 
-cudaError_t setup_prefill_kernels(int* blocks_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(k_route_prefill<DT_F32>,
+template <int DT, bool SPEC>
+static cudaError_t set_prefill_smem(int* bmin) {
+  cudaError_t e = cudaFuncSetAttribute(k_route_prefill<DT, SPEC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PrefillSmem<DT_F32>::total);
+                                       PrefillSmem<DT>::total);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_route_prefill<DT_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PrefillSmem<DT_BF16>::total);
+  int b = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_route_prefill<DT, SPEC>, kPrefillThreads,
+                                                    PrefillSmem<DT>::total);
   if (e != cudaSuccess) return e;
-  int b0 = 0, b1 = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b0, k_route_prefill<DT_F32>, kPrefillThreads,
-                                                    PrefillSmem<DT_F32>::total);
-  if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k_route_prefill<DT_BF16>, kPrefillThreads,
-                                                    PrefillSmem<DT_BF16>::total);
-  if (e != cudaSuccess) return e;
-  *blocks_per_sm = min(b0, b1);
+  *bmin = min(*bmin, b);
   return cudaSuccess;
+}
+
+cudaError_t setup_prefill_kernels(int* blocks_per_sm) {
+  int b = 1 << 30;
+  cudaError_t e;
+  if ((e = set_prefill_smem<DT_F32, false>(&b)) != cudaSuccess) return e;
+  if ((e = set_prefill_smem<DT_F32, true>(&b)) != cudaSuccess) return e;
+  if ((e = set_prefill_smem<DT_BF16, false>(&b)) != cudaSuccess) return e;
+  if ((e = set_prefill_smem<DT_BF16, true>(&b)) != cudaSuccess) return e;
+  *blocks_per_sm = b;
+  return cudaSuccess;
+}
+
+bool prefill_fits(int T, int grid) {
+  // per-warp 16-bit counters: a warp's rows must stay below 65,536
+  if (grid < 1) return false;
+  const long long rows_cta = (static_cast<long long>(T) + grid - 1) / grid;
+  return (rows_cta + kPrefillWarps - 1) / kPrefillWarps < 65536;
 }
 
 cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,
                                  cudaStream_t st) {
+  if (!prefill_fits(a.T, grid)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kPrefillThreads, 1, 1);
@@ -253,12 +340,15 @@ cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS&
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const bool spec = a.k == 16 && a.Kg == 4;
   if (dtype == DT_BF16) {
     cfg.dynamicSmemBytes = PrefillSmem<DT_BF16>::total;
-    return cudaLaunchKernelEx(&cfg, k_route_prefill<DT_BF16>, a, ws);
+    return spec ? cudaLaunchKernelEx(&cfg, k_route_prefill<DT_BF16, true>, a, ws)
+                : cudaLaunchKernelEx(&cfg, k_route_prefill<DT_BF16, false>, a, ws);
   }
   cfg.dynamicSmemBytes = PrefillSmem<DT_F32>::total;
-  return cudaLaunchKernelEx(&cfg, k_route_prefill<DT_F32>, a, ws);
+  return spec ? cudaLaunchKernelEx(&cfg, k_route_prefill<DT_F32, true>, a, ws)
+              : cudaLaunchKernelEx(&cfg, k_route_prefill<DT_F32, false>, a, ws);
 }
 
 }  // namespace moe

@@ -4,16 +4,19 @@
 //   s = sigmoid(x), b = s + bias                    lane l owns experts [28 l, 28 l + 28)
 //   group score = top-2 sum of b over 112 experts   lane top-2, then a 4-lane merge
 //   keep topk_group groups                          rank of each group among the 8 scores
-//   top-k of b over kept experts, ties to lower id  threshold + compaction + warp argmax
+//   top-k of b over kept experts, ties to lower id  threshold + compaction + ranks
 //   weights, relabel, pack                          lanes 0..k-1 hold slots 0..k-1
 //
 // Selection.  tau0 = the k-th largest value of a pool made of the two largest b of
-// every kept lane (a subset of the candidates, so at least k candidates reach tau0).
+// every kept lane (a subset of the candidates, so at least k candidates reach tau0),
+// found by rank counting: each lane counts the pool values above its own.
 // Candidates with b >= tau0 ("survivors", typically 17-22 for k = 16) are compacted
-// one per lane in expert-id order and sorted by one bitonic network on 32-bit keys
-// (b relative to tau0, then position), so exact ties go to the lower id; when the key
-// range does not allow that, k rounds of a warp maximum pick the slots.  If more than
-// 32 survive, a slower exact path extracts the k winners from per-lane maxima.
+// one per lane in expert-id order with 32-bit keys (b relative to tau0, then position,
+// so exact ties go to the lower id); a survivor's slot is the number of larger keys.
+// When the key range does not allow such keys, k rounds of a warp maximum pick the
+// slots.  If more than 32 survive, a slower exact path extracts the k winners from
+// per-lane maxima.  Rank counting reads the pool and the keys from shared memory, so
+// its latency is a few loads instead of a chain of shuffles.
 #pragma once
 #include "common.cuh"
 
@@ -86,6 +89,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Inverse of fkey.
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Adds the pair (u, v) to the top-2 list (m1 >= m2); counts equal values with
 // multiplicity.
 __device__ __forceinline__ void top2_pair(float& m1, float& m2, float u, float v) {
@@ -94,38 +102,50 @@ __device__ __forceinline__ void top2_pair(float& m1, float& m2, float u, float v
   m1 = fmaxf(m1, hi);
 }
 
-// Bitonic compare-exchange across lanes: keeps the larger value in the lane that the
-// network's direction assigns it to.
-template <typename V>
-__device__ __forceinline__ V bitonic_step(V v, int lane, int size, int stride) {
-  const V o = __shfl_xor_sync(0xffffffffu, v, stride);
-  const bool desc = (lane & size) == 0;
-  const bool lower = (lane & stride) == 0;
-  return (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
+// bfloat16 logits: the scores of the two bf16 values packed in v (low half first).
+// Both table indices are formed at once in 16-bit lanes: magnitude clamped to the
+// table's range, plus the entries of one sign (N) for negative values.  `tab_lo` is the
+// table shifted down by the first magnitude it covers, so it is indexed by magnitude.
+__device__ __forceinline__ void sig_bf16_pair(const float* tab_lo, uint32_t v, float& s0, float& s1) {
+  uint32_t m = v & 0x7FFF7FFFu;
+  m = __vmaxu2(m, kSigLo * 0x10001u);
+  m = __vminu2(m, kSigHi * 0x10001u);
+  uint32_t neg;  // 0xFFFF in each half whose sign bit is set
+  asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(neg) : "r"(v));
+  const uint32_t i2 = m + (neg & (uint32_t(kSigN) * 0x10001u));
+  s0 = tab_lo[i2 & 0xFFFFu];
+  s1 = tab_lo[i2 >> 16];
 }
 
 // Routes one row.  `row` points to the row's E logits (or scores) in shared memory
-// (16-byte aligned).  All 32 lanes must call it.
-template <int DT>
+// (16-byte aligned).  All 32 lanes must call it.  KC and KGC fix k and topk_group at
+// compile time (the Kimi-K3 instance: 16 and 4); 0 reads them from `a`.
+template <int DT, int KC = 0, int KGC = 0>
 __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[kEPL],
                                              const float* stab, const RouteArgs& a,
                                              WarpScratch& ws) {
   const unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int e0 = lane * kEPL;
+  const int k = KC ? KC : a.k;
+  const int Kg = KGC ? KGC : a.Kg;
 
   // ---- a1, a2: scores, biased scores, lane top-2 (two independent lists)
   float b[kEPL];
   float xa1 = -INFINITY, xa2 = -INFINITY, xb1 = -INFINITY, xb2 = -INFINITY;
   if constexpr (DT == DT_BF16) {
+    const float* tab_lo = stab - kSigLo;
     const uint2* p = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(row) + e0);
 #pragma unroll
     for (int q = 0; q < kEPL / 4; ++q) {
       const uint2 v = p[q];
-      b[4 * q + 0] = __fadd_rn(sig_bf16(stab, v.x & 0xFFFFu), bl[4 * q + 0]);
-      b[4 * q + 1] = __fadd_rn(sig_bf16(stab, v.x >> 16), bl[4 * q + 1]);
-      b[4 * q + 2] = __fadd_rn(sig_bf16(stab, v.y & 0xFFFFu), bl[4 * q + 2]);
-      b[4 * q + 3] = __fadd_rn(sig_bf16(stab, v.y >> 16), bl[4 * q + 3]);
+      float s0, s1, s2, s3;
+      sig_bf16_pair(tab_lo, v.x, s0, s1);
+      sig_bf16_pair(tab_lo, v.y, s2, s3);
+      b[4 * q + 0] = __fadd_rn(s0, bl[4 * q + 0]);
+      b[4 * q + 1] = __fadd_rn(s1, bl[4 * q + 1]);
+      b[4 * q + 2] = __fadd_rn(s2, bl[4 * q + 2]);
+      b[4 * q + 3] = __fadd_rn(s3, bl[4 * q + 3]);
       top2_pair(xa1, xa2, b[4 * q + 0], b[4 * q + 1]);
       top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
     }
@@ -166,9 +186,9 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
     const float o = __shfl_sync(FULL, gs, g * kLanesPerGroup);
     grank += (o > gs || (o == gs && g < my_g)) ? 1 : 0;
   }
-  const bool kept = grank < a.Kg;
+  const bool kept = grank < Kg;
   const uint32_t kept_lanes = __ballot_sync(FULL, kept);
-  const int nk = __popc(kept_lanes);
+  const int nk = KGC ? KGC * kLanesPerGroup : __popc(kept_lanes);
   const int ki = __popc(kept_lanes & ((1u << lane) - 1u));
 
   // kept lanes park their biased scores for the survivor extraction below
@@ -179,17 +199,22 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
       d[q] = make_float4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
   }
 
-  // ---- a5: threshold tau0 = k-th largest of the pool of kept lanes' top-2
-  ws.pool[lane] = -INFINITY;
-  __syncwarp();
+  // ---- a5: threshold tau0 = k-th largest (with multiplicity) of a pool of candidates
+  //      made of the kept lanes' two largest values; at least k candidates reach it.
+  //      Rank counting: lane l holds pool[l]; tau0 is the smallest pool value with at
+  //      most k - 1 pool values strictly above it.
   int pool_n;
   if (2 * nk <= 32) {
+    if (!KGC || 2 * nk < 32) ws.pool[lane] = -INFINITY;
+    __syncwarp();
     if (kept) {
       ws.pool[2 * ki] = lm1;
       ws.pool[2 * ki + 1] = lm2;
     }
     pool_n = 2 * nk;
   } else {
+    ws.pool[lane] = -INFINITY;
+    __syncwarp();
     if (kept) {
       ws.pool[ki] = lm1;
       if (ki < 32 - nk) ws.pool[nk + ki] = lm2;
@@ -198,33 +223,20 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   }
   __syncwarp();
   float tau0 = -INFINITY;
-  if (pool_n >= a.k) {
-    float v = ws.pool[lane];
-    if (a.k <= 16) {
-      // sort each half of 16 in opposite directions, keep the larger of each pair:
-      // lanes 0..15 then hold the pool's 16 largest values
+  if (pool_n >= k) {
+    const float v = ws.pool[lane];
+    const float4* p4 = reinterpret_cast<const float4*>(ws.pool);
+    int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
 #pragma unroll
-      for (int size = 2; size <= 16; size <<= 1)
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) v = bitonic_step(v, lane, size, stride);
-      v = fmaxf(v, __shfl_xor_sync(FULL, v, 16));
-      if (a.k == 16) {
-        float mn = v;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) mn = fminf(mn, __shfl_xor_sync(FULL, mn, o));
-        tau0 = __shfl_sync(FULL, mn, 0);
-      } else {
-#pragma unroll
-        for (int stride = 8; stride > 0; stride >>= 1) v = bitonic_step(v, lane & 15, 32, stride);
-        tau0 = __shfl_sync(FULL, v, a.k - 1);
-      }
-    } else {
-#pragma unroll
-      for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) v = bitonic_step(v, lane, size, stride);
-      tau0 = __shfl_sync(FULL, v, a.k - 1);
+    for (int q = 0; q < 8; ++q) {
+      const float4 u = p4[q];
+      g0 += u.x > v;
+      g1 += u.y > v;
+      g2 += u.z > v;
+      g3 += u.w > v;
     }
+    const uint32_t cand = (g0 + g1 + g2 + g3 <= k - 1) ? fkey(v) : 0xFFFFFFFFu;
+    tau0 = fkey_inv(__reduce_min_sync(FULL, cand));
   }
 
   uint32_t smask = 0;
@@ -243,16 +255,12 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   __syncwarp();  // ws.b visible to the warp
 
   // composite 32-bit keys (b, position) need tau0 > 0 and survivors within 2^26 float
-  // steps of it; otherwise order keys and k rounds of a warp maximum
-  const bool fast = total <= 32 && tau0 > 0.0f;
-  uint32_t bmax_all = 0;
-  if (fast) {
-    float m = kept ? lm1 : 0.0f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
-    bmax_all = __float_as_uint(m);
+  // steps of it (b >= 0 there, so float bits order like the values)
+  bool keys32 = false;
+  if (total <= 32 && tau0 > 0.0f) {
+    const uint32_t bmax = __reduce_max_sync(FULL, kept ? __float_as_uint(lm1) : 0u);
+    keys32 = (bmax - __float_as_uint(tau0)) < (1u << 26);
   }
-  const bool keys32 = fast && (bmax_all - __float_as_uint(tau0)) < (1u << 26);
 
   if (total <= 32) {
     int pos = incl - c;
@@ -268,17 +276,24 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
     }
     __syncwarp();
     if (keys32) {
-      // one bitonic sort of (b, position) keys: slot j = lane j after the sort
-      uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
+      // unique keys: a survivor's slot is the number of survivors with a larger key
+      const uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
+      const uint4* k4 = reinterpret_cast<const uint4*>(ws.skey);
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
 #pragma unroll
-      for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) key = bitonic_step(key, lane, size, stride);
-      if (lane < a.k) ws.slot_id[lane] = ws.sid[31 - int(key & 31u)];
+      for (int q = 0; q < 8; ++q) {
+        const uint4 u = k4[q];
+        r0 += (4 * q + 0 < total) & (u.x > key);
+        r1 += (4 * q + 1 < total) & (u.y > key);
+        r2 += (4 * q + 2 < total) & (u.z > key);
+        r3 += (4 * q + 3 < total) & (u.w > key);
+      }
+      const int rank = r0 + r1 + r2 + r3;
+      if (lane < total && rank < k) ws.slot_id[rank] = ws.sid[lane];
     } else {
       uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
       const int my_id = (lane < total) ? ws.sid[lane] : 0;
-      for (int j = 0; j < a.k; ++j) {
+      for (int j = 0; j < k; ++j) {
         const uint32_t top = __reduce_max_sync(FULL, key);
         const int win = __ffs(__ballot_sync(FULL, key == top)) - 1;
         if (lane == win) {
@@ -306,7 +321,7 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
     uint32_t bk;
     int bi;
     lane_best(bk, bi);
-    for (int j = 0; j < a.k; ++j) {
+    for (int j = 0; j < k; ++j) {
       const uint32_t top = __reduce_max_sync(FULL, bk);
       const int win = __ffs(__ballot_sync(FULL, bk == top)) - 1;
       if (lane == win) {
@@ -324,13 +339,15 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   out.lid = 0;
   out.packed = 0;
   float s = 0.0f;
-  if (lane < a.k) {
+  if (lane < k) {
     out.id = ws.slot_id[lane];
     s = row_sigmoid<DT>(row, out.id, stab, a.etab);
   }
+  // sequential sum in slot order; lanes >= k hold s = 0, and adding +0 to den > 0 is exact
   float den = 0.0f;
-  for (int j = 0; j < a.k; ++j) den = __fadd_rn(den, __shfl_sync(FULL, s, j));
-  if (lane < a.k) {
+#pragma unroll
+  for (int j = 0; j < (KC ? KC : kMaxK); ++j) den = __fadd_rn(den, __shfl_sync(FULL, s, j));
+  if (lane < k) {
     const float w = __fmul_rn(__fdiv_rn(s, den), a.scale);
     const uint32_t wb = f32_to_bf16_bits(w);
     int lid = out.id;

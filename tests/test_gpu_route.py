@@ -131,6 +131,15 @@ def test_cfg4_ties_f32(mr, off, cnt):
     assert rep["mismatched_rows"] <= rep.get("near_tie_rows", 0)
 
 
+@pytest.mark.parametrize("T,path", [(64, 1), (3000, 2)])
+@pytest.mark.parametrize("off,cnt", [(0, 0), (448, 112)])
+def test_every_bf16_magnitude(mr, T, path, off, cnt):
+    """bf16 logits over all finite bit patterns (zeros, subnormals, magnitudes below
+    2^-26 and above 112, both signs) reach the clamped score-table lookups of the row
+    routine on both paths; many exact ties in b."""
+    check(mr, gen.cfg_bf16_patterns(T, off=off, cnt=cnt), exact=True, path=path)
+
+
 def test_t_zero(mr):
     cfg = gen.cfg1(8)
     lg, bias = to_dev(cfg)
