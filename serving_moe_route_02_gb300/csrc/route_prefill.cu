@@ -271,28 +271,42 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   }
   for (int e = tid; e < a.NE; e += kPrefillThreads) base_s[e] += __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
   __syncthreads();
-  if (lane < a.k) {
-    // rows in order; packed ids are loaded eight rows ahead of their use
-    int* wpre = wpre_all + w * kMaxBins;
-    const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
-    constexpr int kAhead = 8;
-    int32_t x[kAhead];
+  // The walk: this warp's packed ids are staged in its (now free) routing scratch, a
+  // chunk of rows at a time, with all loads of a chunk in flight at once; the rows are
+  // then taken in order from shared memory.
+  int* wpre = wpre_all + w * kMaxBins;
+  int* stage = reinterpret_cast<int*>(wsp + w);
+  constexpr int kStageInts = int(sizeof(WarpScratch)) / 4;
+  const int chunk_rows = kStageInts / a.k;
+  const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
+  for (int c0 = 0; c0 < nw; c0 += chunk_rows) {
+    const int nr = min(chunk_rows, nw - c0);
+    const int n = nr * a.k;
+    const int32_t* src = a.packed + size_t(wr0 + c0) * a.k;
+    for (int i0 = 0; i0 < n; i0 += 8 * 32) {
+      int32_t v[8];
 #pragma unroll
-    for (int q = 0; q < kAhead; ++q) x[q] = (q < nw) ? a.packed[size_t(wr0 + q) * a.k + lane] : 0;
-    for (int i0 = 0; i0 < nw; i0 += kAhead) {
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * 32 + lane;
+        v[q] = (i < n) ? src[i] : 0;
+      }
 #pragma unroll
-      for (int q = 0; q < kAhead; ++q) {
-        const int i = i0 + q;
-        if (i < nw) {
-          const int l = int(uint32_t(x[q]) >> 16);
-          const int r = wpre[l];
-          wpre[l] = r + 1;
-          a.perm[base_s[l] + r] = (wr0 + i) * a.k + lane;
-          x[q] = (i + kAhead < nw) ? a.packed[size_t(wr0 + i + kAhead) * a.k + lane] : 0;
-        }
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * 32 + lane;
+        if (i < n) stage[i] = v[q];
+      }
+    }
+    __syncwarp();
+    if (lane < a.k) {
+      for (int r = 0; r < nr; ++r) {
+        const int l = int(uint32_t(stage[r * a.k + lane]) >> 16);
+        const int rk = wpre[l];
+        wpre[l] = rk + 1;
+        a.perm[base_s[l] + rk] = (wr0 + c0 + r) * a.k + lane;
         __syncwarp(kmask);  // the next row may count the same bin in another lane
       }
     }
+    __syncwarp();
   }
 }
 
