@@ -263,6 +263,7 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   }
 
   if (total <= 32) {
+    if (keys32 && lane >= total) ws.skey[lane] = 0u;  // below every survivor's key
     int pos = incl - c;
     while (smask) {
       const int i = __ffs(smask) - 1;
@@ -277,16 +278,27 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
     __syncwarp();
     if (keys32) {
       // unique keys: a survivor's slot is the number of survivors with a larger key
-      const uint32_t key = (lane < total) ? ws.skey[lane] : 0u;
+      // (slots past `total` hold 0, below every key; almost always total <= 24)
+      const uint32_t key = ws.skey[lane];
       const uint4* k4 = reinterpret_cast<const uint4*>(ws.skey);
       int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+      for (int q = 0; q < 6; ++q) {
         const uint4 u = k4[q];
-        r0 += (4 * q + 0 < total) & (u.x > key);
-        r1 += (4 * q + 1 < total) & (u.y > key);
-        r2 += (4 * q + 2 < total) & (u.z > key);
-        r3 += (4 * q + 3 < total) & (u.w > key);
+        r0 += u.x > key;
+        r1 += u.y > key;
+        r2 += u.z > key;
+        r3 += u.w > key;
+      }
+      if (total > 24) {
+#pragma unroll
+        for (int q = 6; q < 8; ++q) {
+          const uint4 u = k4[q];
+          r0 += u.x > key;
+          r1 += u.y > key;
+          r2 += u.z > key;
+          r3 += u.w > key;
+        }
       }
       const int rank = r0 + r1 + r2 + r3;
       if (lane < total && rank < k) ws.slot_id[rank] = ws.sid[lane];
@@ -343,10 +355,19 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
     out.id = ws.slot_id[lane];
     s = row_sigmoid<DT>(row, out.id, stab, a.etab);
   }
-  // sequential sum in slot order; lanes >= k hold s = 0, and adding +0 to den > 0 is exact
+  // sequential sum in slot order, read back from shared memory; lanes >= k hold s = 0,
+  // and adding +0 to den > 0 is exact
+  ws.pool[lane] = s;
+  __syncwarp();
   float den = 0.0f;
+  {
+    const float4* s4 = reinterpret_cast<const float4*>(ws.pool);
 #pragma unroll
-  for (int j = 0; j < (KC ? KC : kMaxK); ++j) den = __fadd_rn(den, __shfl_sync(FULL, s, j));
+    for (int q = 0; q < (KC ? (KC + 3) / 4 : kMaxK / 4); ++q) {
+      const float4 u = s4[q];
+      den = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(den, u.x), u.y), u.z), u.w);
+    }
+  }
   if (lane < k) {
     const float w = __fmul_rn(__fdiv_rn(s, den), a.scale);
     const uint32_t wb = f32_to_bf16_bits(w);
