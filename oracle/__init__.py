@@ -60,6 +60,8 @@ def _bind(lib):
     lib.oracle_route.restype = I
     lib.oracle_router_gemm.argtypes = [P, P, I, I, I, P]
     lib.oracle_router_gemm.restype = None
+    lib.oracle_route_layout.argtypes = [P, P, P, I, I, I, I, P, P, P, P]
+    lib.oracle_route_layout.restype = I
     return lib
 
 
@@ -121,3 +123,25 @@ def router_gemm(hidden: np.ndarray, w: np.ndarray, lib=None) -> np.ndarray:
     out = np.zeros((T, E), dtype=np.float64)
     lib.oracle_router_gemm(_ptr(h), _ptr(ww), T, H, E, _ptr(out))
     return out
+
+
+def route_layout(counts: np.ndarray, offsets: np.ndarray, perm: np.ndarray, tile: int,
+                 capacity: int | None = None, lib=None) -> dict:
+    """Inverse permutation, padded offsets, padded rows and m_indices of a routing
+    result (see oracle_route_layout).  capacity defaults to the padded total's bound
+    n + NE * (tile - 1)."""
+    counts = np.ascontiguousarray(counts, dtype=np.int32)
+    offsets = np.ascontiguousarray(offsets, dtype=np.int32)
+    perm = np.ascontiguousarray(perm, dtype=np.int32).ravel()
+    NE, n = counts.size, perm.size
+    cap = n + NE * (tile - 1) if capacity is None else capacity
+    inv = np.empty(n, np.int32)
+    poff = np.empty(NE + 1, np.int32)
+    rows = np.empty(max(cap, 0), np.int32)
+    mind = np.empty(max(cap, 0), np.int32)
+    total = (lib or load()).oracle_route_layout(_ptr(counts), _ptr(offsets), _ptr(perm), n, NE,
+                                                tile, cap, _ptr(inv), _ptr(poff), _ptr(rows),
+                                                _ptr(mind))
+    if total < 0:
+        raise ValueError("oracle_route_layout rejected its arguments")
+    return dict(inv_perm=inv, padded_offsets=poff, padded_rows=rows, m_indices=mind, total=total)

@@ -199,3 +199,43 @@ void oracle_router_gemm(const uint16_t* hidden, const uint16_t* w, int T, int H,
             logits[(size_t)t * E + e] = acc;
         }
 }
+
+int oracle_route_layout(const int32_t* counts, const int32_t* offsets, const int32_t* perm, int n,
+                        int NE, int tile, int capacity, int32_t* inv_perm, int32_t* padded_offsets,
+                        int32_t* padded_rows, int32_t* m_indices) {
+    if (n < 0 || NE < 1 || tile < 1 || capacity < 0) return -1;
+    /* inverse permutation: the entry perm[p] sits at position p */
+    if (inv_perm)
+        for (int p = 0; p < n; ++p) inv_perm[perm[p]] = p;
+    /* padded offsets: each bin's block rounded up to a multiple of the tile */
+    int32_t* poff = (int32_t*)malloc(sizeof(int32_t) * (size_t)(NE + 1));
+    long long total = 0;
+    poff[0] = 0;
+    for (int e = 0; e < NE; ++e) {
+        long long blocks = ((long long)counts[e] + tile - 1) / tile;
+        total += blocks * tile;
+        if (total > 0x7FFFFFFFLL) {
+            free(poff);
+            return -1;
+        }
+        poff[e + 1] = (int32_t)total;
+    }
+    if (padded_offsets)
+        for (int e = 0; e <= NE; ++e) padded_offsets[e] = poff[e];
+    if ((padded_rows || m_indices) && total > capacity) {
+        free(poff);
+        return -1;
+    }
+    /* padded rows: every row starts as padding, then each bin's entries in perm order */
+    for (int r = 0; r < capacity; ++r) {
+        if (padded_rows) padded_rows[r] = -1;
+        if (m_indices) m_indices[r] = -1;
+    }
+    for (int e = 0; e < NE; ++e)
+        for (int i = 0; i < counts[e]; ++i) {
+            if (padded_rows) padded_rows[poff[e] + i] = perm[offsets[e] + i];
+            if (m_indices) m_indices[poff[e] + i] = e;
+        }
+    free(poff);
+    return (int)total;
+}

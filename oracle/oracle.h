@@ -70,6 +70,22 @@ int oracle_route(const void* logits, int dtype, const float* bias, int T, int E,
 void oracle_router_gemm(const uint16_t* hidden, const uint16_t* w, int T, int H, int E,
                         double* logits);
 
+/* Layout of the routed entries for grouped expert GEMMs, from the routing outputs
+ * counts [NE], offsets [NE + 1] and perm [n] (n = T * k).  The pages only name these
+ * structures (an expert-GEMM row index built from the routing -- InferenceX PR #2453,
+ * review summary of the MoonEP backend; the entries reaching the expert GEMMs in the
+ * routing's order -- sglang PR #37, description); the plainest reading is taken:
+ *   inv_perm[perm[p]] = p                     (the inverse permutation)
+ *   padded_offsets[0] = 0,
+ *   padded_offsets[e + 1] = padded_offsets[e] + round_up(counts[e], tile)
+ *   padded row padded_offsets[e] + i, i < counts[e]: padded_rows = perm[offsets[e] + i]
+ *   and m_indices = e; every other row r < capacity holds -1 in both.
+ * Any output may be NULL.  Returns padded_offsets[NE], or -1 for an invalid argument
+ * (tile < 1, or capacity below the padded total when a padded array is asked for). */
+int oracle_route_layout(const int32_t* counts, const int32_t* offsets, const int32_t* perm, int n,
+                        int NE, int tile, int capacity, int32_t* inv_perm, int32_t* padded_offsets,
+                        int32_t* padded_rows, int32_t* m_indices);
+
 #ifdef __cplusplus
 }
 #endif

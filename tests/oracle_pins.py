@@ -11,7 +11,10 @@ AssertionError when the oracle disagrees with:
   * invariants stated for the method (unique ids, ids inside kept groups,
     counts summing to T*k, perm a permutation, weights summing to the scale,
     rank-local ids unique, < count+k, round-tripping to the global ids),
-  * facts printed on the pages (num_experts 128 at EP8, router size).
+  * facts printed on the pages (num_experts 128 at EP8, router size),
+  * for the expert-GEMM layout: numpy's argsort (inverse permutation), numpy.repeat
+    (unpadded row index), a padded layout built by appending entries and padding,
+    and its invariants.
 The same functions are run against deliberately broken copies of the oracle in
 test_oracle_mutations.py to show that each plausible mistake is caught.
 """
@@ -385,9 +388,101 @@ def pin_rejects_invalid(lib):
         raise AssertionError(f"oracle accepted {b}")
 
 
+def _layout_cases(lib):
+    """Routing results the layout pins start from: decode, rank-local, ties, tiny."""
+    for cfg in (gen.cfg1(8), gen.cfg1(64, off=0, cnt=0), gen.cfg4(T=300, n_hot=80, off=224, cnt=112),
+                small_cfg(T=40, E=32, G=4, Kg=2, k=4, seed=95), small_cfg(T=1, E=8, G=2, Kg=1, k=2, seed=96)):
+        out = run(lib, cfg)
+        yield cfg, out
+
+
+def layout(lib, out, tile, capacity=None):
+    return oracle.route_layout(out["counts"], out["offsets"], out["perm"], tile, capacity, lib=lib)
+
+
+def pin_layout_inverse(lib):
+    """inv_perm is the inverse permutation: numpy's argsort of perm, and perm[inv] = id."""
+    for _, out in _layout_cases(lib):
+        L = layout(lib, out, 8)
+        n = out["perm"].size
+        assert np.array_equal(L["inv_perm"], np.argsort(out["perm"], kind="stable"))
+        assert np.array_equal(out["perm"][L["inv_perm"]], np.arange(n))
+
+
+def pin_layout_tile_one(lib):
+    """tile = 1 is the unpadded layout: padded offsets = offsets, padded rows = perm,
+    m_indices = numpy.repeat of the bins by their counts, nothing else written."""
+    for _, out in _layout_cases(lib):
+        n, NE = out["perm"].size, out["counts"].size
+        L = layout(lib, out, 1, capacity=n + 5)
+        assert L["total"] == n
+        assert np.array_equal(L["padded_offsets"], out["offsets"])
+        assert np.array_equal(L["padded_rows"][:n], out["perm"])
+        assert np.array_equal(L["m_indices"][:n], np.repeat(np.arange(NE), out["counts"]))
+        assert np.all(L["padded_rows"][n:] == -1) and np.all(L["m_indices"][n:] == -1)
+
+
+def pin_layout_append(lib):
+    """Padded layout built by a different method: append each bin's entries, then -1
+    until the length is a multiple of the tile; pad to the capacity with -1."""
+    for _, out in _layout_cases(lib):
+        lid, _ = unpack(out["packed"])
+        flat = lid.ravel()
+        NE = out["counts"].size
+        for tile in (2, 3, 8, 128):
+            rows, mind, starts = [], [], []
+            for e in range(NE):
+                starts.append(len(rows))
+                for x in range(flat.size):      # entries of bin e in (token, slot) order
+                    if flat[x] == e:
+                        rows.append(x)
+                        mind.append(e)
+                while len(rows) % tile:
+                    rows.append(-1)
+                    mind.append(-1)
+            starts.append(len(rows))
+            cap = len(rows) + 7
+            L = layout(lib, out, tile, capacity=cap)
+            assert L["total"] == len(rows)
+            assert np.array_equal(L["padded_offsets"], np.array(starts))
+            assert np.array_equal(L["padded_rows"], np.array(rows + [-1] * 7))
+            assert np.array_equal(L["m_indices"], np.array(mind + [-1] * 7))
+
+
+def pin_layout_invariants(lib):
+    """Every block is the smallest multiple of the tile that holds its bin; a real padded
+    row's entry carries the bin's id in its packed value; the padded total is within the
+    bound n + NE (tile - 1) that callers size their buffers by."""
+    for _, out in _layout_cases(lib):
+        lid, _ = unpack(out["packed"])
+        flat = lid.ravel()
+        n, NE = flat.size, out["counts"].size
+        for tile in (4, 16, 128):
+            L = layout(lib, out, tile)
+            size = np.diff(L["padded_offsets"])
+            assert np.all(size % tile == 0)
+            assert np.all(size >= out["counts"]) and np.all(size < out["counts"] + tile)
+            assert L["total"] <= n + NE * (tile - 1)
+            real = L["padded_rows"] >= 0
+            assert real.sum() == n
+            assert np.array_equal(flat[L["padded_rows"][real]], L["m_indices"][real])
+            assert np.all(L["m_indices"][~real] == -1)
+
+
+def pin_layout_rejects(lib):
+    out = run(lib, gen.cfg1(8))
+    for tile, cap in ((0, 1000), (8, 10)):
+        try:
+            layout(lib, out, tile, capacity=cap)
+        except ValueError:
+            continue
+        raise AssertionError(f"layout accepted tile={tile} capacity={cap}")
+
+
 ALL_PINS = [
     pin_sigmoid_exact, pin_sigmoid_symmetry, pin_bf16_rounding, pin_selection_brute_force,
     pin_selection_exhaustive, pin_selection_kimi_shape, pin_plain_topk, pin_keep_all_groups_is_noop,
     pin_weights, pin_histogram_scan_perm, pin_invariants, pin_rank_local_matrix, pin_page_facts,
-    pin_router_gemm, pin_rejects_invalid,
+    pin_router_gemm, pin_rejects_invalid, pin_layout_inverse, pin_layout_tile_one, pin_layout_append,
+    pin_layout_invariants, pin_layout_rejects,
 ]

@@ -47,6 +47,14 @@ MUTANTS = {
                                "(double)f32_from_bf16(w[(size_t)h * E + e]);"),
     "num_experts_no_roundup": ("return ((local_count + k + 3) / 4) * 4;",
                                "return local_count + k;"),
+    "layout_inverse_transposed": ("for (int p = 0; p < n; ++p) inv_perm[perm[p]] = p;",
+                                  "for (int p = 0; p < n; ++p) inv_perm[p] = perm[p];"),
+    "layout_round_down": ("long long blocks = ((long long)counts[e] + tile - 1) / tile;",
+                          "long long blocks = ((long long)counts[e]) / tile;"),
+    "layout_pad_zero": ("        if (padded_rows) padded_rows[r] = -1;",
+                        "        if (padded_rows) padded_rows[r] = 0;"),
+    "layout_bin_index_shifted": ("            if (m_indices) m_indices[poff[e] + i] = e;",
+                                 "            if (m_indices) m_indices[poff[e] + i] = e + 1;"),
 }
 
 # cheap pins first; the exhaustive sigmoid sweep last
