@@ -8,7 +8,8 @@ call over the whole batch: scores, grouped top-k, weights, pack, histogram, scan
 the stable permutation (one kernel launch).  value = routed tokens/s over all ranks.
 
 Also reported (same JSON line): decode routing latency at 8-64 rows (rank-local ids,
-CUDA-graph replay) against an empty-kernel floor replayed the same way, a roofline
+CUDA-graph replay) against an empty-kernel floor replayed the same way, the router
+contraction + routing at 1-64 rows, the expert-GEMM layout at 65,536 rows, a roofline
 object for the prefill kernel, the CPU oracle's throughput on the machine's host, an
 end-to-end number with host buffers, and SM clocks sampled during the timed region.
 
@@ -296,6 +297,39 @@ def gemm_route_latency(torch, mr, dev, reps=100, replays=10):
     return res
 
 
+def layout_timing(torch, mr, dev, out, T, tile=128, reps=50):
+    """moe_route_layout at T rows (global ids, one call per step): µs per call and the
+    HBM bandwidth of its algorithmic bytes (perm read once, inverse written, padded rows
+    and m_indices written over the whole capacity)."""
+    L = mr.route_layout(out, tile)
+    torch.cuda.synchronize()
+    n = T * K
+    NE = out["counts"].numel()
+    cap = L["padded_rows"].numel()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        mr.route_layout(out, tile, layout=L)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / reps
+    Lp = dict(L, inv_perm=None)
+    a.record()
+    for _ in range(reps):
+        mr.route_layout(out, tile, layout=Lp)
+    b.record()
+    torch.cuda.synchronize()
+    us_padded = a.elapsed_time(b) * 1e3 / reps
+    nbytes = 4 * n + 4 * n + 2 * 4 * cap + 4 * (2 * NE + 1) + 4 * (NE + 1)
+    peaks, _ = measured_peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"T": T, "tile": tile, "capacity": cap, "us_per_call": round(us, 3),
+            "us_per_call_without_inverse": round(us_padded, 3),
+            "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
+            "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
+
+
 def run_case(torch, mr, dev, args, T=64):
     """Plain launches of one decode-size path, for ncu captures."""
     if args.case == "decode":
@@ -459,10 +493,11 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt[0])
 
-    decode = gemm = None
+    decode = gemm = layout = None
     if rank == 0 and not (args.no_decode or args.quick):
         decode = decode_latency(torch, mr, dev)
         gemm = gemm_route_latency(torch, mr, dev)
+        layout = layout_timing(torch, mr, dev, outs[0], T_PREFILL)
 
     peaks, peak_src = measured_peaks()
     ab = algorithmic_bytes(T_PREFILL)
@@ -498,6 +533,8 @@ def main():
         line["decode"] = decode
     if gemm is not None:
         line["router_gemm_route"] = gemm
+    if layout is not None:
+        line["route_layout"] = layout
     if rank == 0 and not (args.no_cpu_baseline or args.quick):
         line["cpu_baseline"] = cpu_baseline()
     if world > 1:

@@ -105,6 +105,43 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
                           int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* topk_ids,
                           struct CUstream_st* stream);
 
+/*
+ * moe_route_layout -- the layout of the routed entries that grouped expert GEMMs consume,
+ * built from the outputs of moe_route (or moe_router_gemm_route) on the same stream.
+ * The pages name these structures without defining them: an expert-GEMM row index
+ * built from the routing (InferenceX PR #2453, review summary of the MoonEP backend:
+ * a kernel building DeepGEMM's m_indices) and the routed entries reaching the expert
+ * GEMMs in the routing's order (sglang PR #37, description).  Definitions taken:
+ *   inv_perm[perm[p]] = p                     (where entry t*k + j went; for the combine)
+ *   padded_offsets[0] = 0,
+ *   padded_offsets[e + 1] = padded_offsets[e] + round_up(counts[e], tile)
+ *   padded row padded_offsets[e] + i, i < counts[e]:  padded_rows = perm[offsets[e] + i]
+ *                                                      m_indices   = e
+ *   every other row r < capacity:                     padded_rows = m_indices = -1
+ * so each bin occupies whole tiles of `tile` rows, as a grouped GEMM with M-tiles of
+ * that height expects (tile = 1 gives the unpadded layout).
+ *   counts [NE], offsets [NE + 1], perm [T * k]: device, as moe_route wrote them
+ *               (NE = moe_route_bins(E, k, local_count)); perm must be a permutation.
+ *   tile >= 1.
+ *   inv_perm [T * k], padded_offsets [NE + 1]: device outputs, nullable.
+ *   padded_rows [capacity], m_indices [capacity]: device outputs, nullable; when either
+ *               is given, capacity >= moe_route_padded_capacity(T, k, NE, tile), which
+ *               bounds the padded total for any counts, so buffers sized once serve
+ *               every call (CUDA graphs).  All `capacity` rows are written.
+ * Errors: INVALID_ARG for T < 0, k < 1, NE < 1, tile < 1, a NULL counts/offsets (or
+ * perm with T * k > 0), a capacity below the bound, or a bound beyond 2^31 - 1;
+ * UNSUPPORTED for NE > 1,056.  All outputs NULL: returns OK and enqueues nothing.
+ * One kernel launch; no allocation after the library's per-device state exists.
+ */
+int moe_route_layout(const int32_t* counts, const int32_t* offsets, const int32_t* perm, int T,
+                     int k, int NE, int tile, int32_t* inv_perm, int32_t* padded_offsets,
+                     int32_t* padded_rows, int32_t* m_indices, int capacity,
+                     struct CUstream_st* stream);
+
+/* Rows the padded layout can need for any routing of T rows: T * k + NE * (tile - 1);
+ * MOE_ROUTE_E_INVALID_ARG for invalid arguments or a bound beyond 2^31 - 1. */
+int moe_route_padded_capacity(int T, int k, int NE, int tile);
+
 /* Number of expert bins the outputs use: local_count > 0 ? round_up(local_count + k, 4) : E. */
 int moe_route_bins(int E, int k, int local_count);
 

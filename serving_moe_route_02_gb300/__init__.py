@@ -63,6 +63,10 @@ def load(path: str | None = None):
     lib.moe_route_set_path.restype = I
     lib.moe_route_noalloc.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
     lib.moe_route_noalloc.restype = I
+    lib.moe_route_layout.argtypes = [P, P, P, I, I, I, I, P, P, P, P, I, P]
+    lib.moe_route_layout.restype = I
+    lib.moe_route_padded_capacity.argtypes = [I, I, I, I]
+    lib.moe_route_padded_capacity.restype = I
     lib.moe_route_empty.argtypes = [I, P]
     lib.moe_route_empty.restype = I
     lib.moe_route_strerror.argtypes = [I]
@@ -187,6 +191,39 @@ def router_gemm_route(hidden: torch.Tensor, w_router: torch.Tensor, bias: torch.
                                       _ptr(out.get("ids")), _stream(stream))
     _check(rc, "moe_router_gemm_route")
     return out
+
+
+def padded_capacity(T: int, k: int, NE: int, tile: int) -> int:
+    cap = load().moe_route_padded_capacity(T, k, NE, tile)
+    if cap < 0:
+        raise MoeRouteError(cap, "moe_route_padded_capacity")
+    return cap
+
+
+def route_layout(out: dict, tile: int = 128, *, k: int | None = None, inv: bool = True,
+                 padded: bool = True, layout: dict | None = None, stream=None) -> dict:
+    """moe_route_layout on the outputs `out` of route() / router_gemm_route(): inverse
+    permutation, tile-padded offsets, padded rows and m_indices (device tensors)."""
+    T = out["packed"].shape[0]
+    k = out["packed"].shape[1] if k is None else k
+    NE = out["counts"].numel()
+    dev = out["counts"].device
+    cap = padded_capacity(T, k, NE, tile)
+    if layout is None:
+        layout = dict(
+            inv_perm=torch.empty(T * k, dtype=torch.int32, device=dev) if inv else None,
+            padded_offsets=torch.empty(NE + 1, dtype=torch.int32, device=dev) if padded else None,
+            padded_rows=torch.empty(cap, dtype=torch.int32, device=dev) if padded else None,
+            m_indices=torch.empty(cap, dtype=torch.int32, device=dev) if padded else None)
+    rows = layout.get("padded_rows")
+    mind = layout.get("m_indices")
+    capacity = (rows.numel() if rows is not None else mind.numel()) if (rows is not None or mind is not None) else 0
+    rc = load().moe_route_layout(_ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]), T, k,
+                                 NE, tile, _ptr(layout.get("inv_perm")),
+                                 _ptr(layout.get("padded_offsets")), _ptr(rows), _ptr(mind),
+                                 capacity, _stream(stream))
+    _check(rc, "moe_route_layout")
+    return layout
 
 
 def empty_kernel(ctas: int = 1, stream=None):

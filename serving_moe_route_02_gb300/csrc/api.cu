@@ -224,6 +224,43 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
   return launch_route_decode(a, DT_SCORE, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }
 
+int moe_route_padded_capacity(int T, int k, int NE, int tile) {
+  if (T < 0 || k < 1 || NE < 1 || tile < 1) return MOE_ROUTE_E_INVALID_ARG;
+  const long long cap = static_cast<long long>(T) * k + static_cast<long long>(NE) * (tile - 1);
+  return cap < (1ll << 31) ? static_cast<int>(cap) : MOE_ROUTE_E_INVALID_ARG;
+}
+
+int moe_route_layout(const int32_t* counts, const int32_t* offsets, const int32_t* perm, int T,
+                     int k, int NE, int tile, int32_t* inv_perm, int32_t* padded_offsets,
+                     int32_t* padded_rows, int32_t* m_indices, int capacity,
+                     struct CUstream_st* stream) {
+  const int need = moe_route_padded_capacity(T, k, NE, tile);
+  if (need < 0) return MOE_ROUTE_E_INVALID_ARG;
+  if (NE > kMaxBins) return MOE_ROUTE_E_UNSUPPORTED;
+  const int n = T * k;
+  if (!counts || !offsets || (n > 0 && !perm)) return MOE_ROUTE_E_INVALID_ARG;
+  const bool padded = padded_rows || m_indices;
+  if (padded && capacity < need) return MOE_ROUTE_E_INVALID_ARG;
+  if (!inv_perm && !padded_offsets && !padded) return MOE_ROUTE_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevState* d = nullptr;
+  const int rc = get_state(st, &d);
+  if (rc != MOE_ROUTE_OK) return rc;
+  LayoutArgs g = {};
+  g.counts = counts;
+  g.offsets = offsets;
+  g.perm = perm;
+  g.n = n;
+  g.NE = NE;
+  g.tile = tile;
+  g.capacity = padded ? capacity : 0;
+  g.inv_perm = inv_perm;
+  g.padded_offsets = padded_offsets;
+  g.padded_rows = padded_rows;
+  g.m_indices = m_indices;
+  return launch_route_layout(g, d->nsm, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
+}
+
 int moe_route_device_status(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ROUTE_E_CUDA;

@@ -18,6 +18,19 @@ struct PrefillWS {
 
 constexpr int kSigTablePad = (kSigTable + 3) / 4 * 4;  // table length rounded to 16 bytes
 
+// Arguments of the expert-GEMM layout kernel (route_layout.cu).
+struct LayoutArgs {
+  const int32_t* counts;     // [NE]
+  const int32_t* offsets;    // [NE + 1]
+  const int32_t* perm;       // [n]
+  int n, NE, tile, capacity;
+  int32_t* inv_perm;         // [n] or nullptr
+  int32_t* padded_offsets;   // [NE + 1] or nullptr
+  int32_t* padded_rows;      // [capacity] or nullptr
+  int32_t* m_indices;        // [capacity] or nullptr
+};
+
+cudaError_t launch_route_layout(const LayoutArgs& g, int nsm, cudaStream_t st);
 cudaError_t launch_sigmoid_table(float* tab, float2* etab, cudaStream_t st);
 cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const float2* etab, float* s,
                            int n, cudaStream_t st);
