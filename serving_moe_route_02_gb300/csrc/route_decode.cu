@@ -33,7 +33,8 @@ struct DecodeSmem {
   static constexpr int ROWB = (DT == DT_BF16) ? kE * 2 : kE * 4;
   static constexpr int STAB = (DT == DT_BF16) ? kSigTablePad * 4 : 0;
   static constexpr int o_stab = 0;
-  static constexpr int o_rows = align_up(o_stab + STAB, 128);  // (scores: no table)
+  static constexpr int o_bias = align_up(o_stab + STAB, 128);  // (scores: no table)
+  static constexpr int o_rows = align_up(o_bias + kE * 4, 128);
   static constexpr int o_ws = align_up(o_rows + kDecodeRowsPerCta * ROWB, 128);
   static constexpr int o_lid = align_up(o_ws + kDecodeRowsPerCta * int(sizeof(WarpScratch)), 128);
   static constexpr int o_offs = align_up(o_lid + 64 * kMaxK * 4, 128);  // lid: [64 rows][32]
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   extern __shared__ __align__(128) uint8_t smem[];
   cg::cluster_group cluster = cg::this_cluster();
   float* stab = reinterpret_cast<float*>(smem + L::o_stab);
+  float* bias_s = reinterpret_cast<float*>(smem + L::o_bias);
   uint8_t* rows = smem + L::o_rows;
   WarpScratch* wsp = reinterpret_cast<WarpScratch*>(smem + L::o_ws);
   int* offs_s = reinterpret_cast<int*>(smem + L::o_offs);
@@ -97,7 +99,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   const int nctas = static_cast<int>(cluster.num_blocks());
   const int row0 = crank * kDecodeRowsPerCta;
   const int nrows = max(0, min(kDecodeRowsPerCta, a.T - row0));
-  const uint32_t bytes = uint32_t(nrows) * L::ROWB + uint32_t(L::STAB);
+  const uint32_t bytes = uint32_t(nrows) * L::ROWB + uint32_t(L::STAB) + uint32_t(kE * 4);
   const bool have = nrows > 0;  // CTAs without rows (T = 0) load nothing
 
   if (tid == 0) {
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   if (tid == 0 && have) {
     mbar_expect_tx(mbar, bytes);
     if (L::STAB) bulk_g2s(stab, a.stab, L::STAB, mbar);
+    bulk_g2s(bias_s, a.bias, kE * 4, mbar);
     bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
              uint32_t(nrows) * L::ROWB, mbar);
   }
@@ -116,13 +119,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   // flight), wait after routing
   for (int e = tid; e < a.NE; e += kDecodeThreads) mask_s[e] = 0ull;
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  float bl[kEPL];
-  load_lane_bias(a.bias, bl);
   if (have) mbar_wait_bounded(mbar, 0, a.err);
 
   SlotOut o = {};
   if (w < nrows) {
-    o = route_row<DT, SPEC ? 16 : 0, SPEC ? 4 : 0>(rows + w * L::ROWB, bl, stab, a, wsp[w]);
+    o = route_row<DT, SPEC ? 16 : 0, SPEC ? 4 : 0>(rows + w * L::ROWB, bias_s, stab, a, wsp[w]);
     const int t = row0 + w;
     if (lane < a.k) {
       a.packed[size_t(t) * a.k + lane] = o.packed;

@@ -1,23 +1,23 @@
 // route_prefill.cu -- prefill-size routing (thousands of rows) in one persistent,
-// cooperative launch: one CTA of 16 warps per SM, a contiguous row range per CTA and a
-// contiguous sub-range per warp.
+// cooperative launch: one CTA per SM, a contiguous row range per CTA and a contiguous
+// sub-range per warp.  The bf16 Kimi-K3 instance (k = 16, keep 4 groups) runs 24 warps
+// per SM (scratch sized for 448 kept candidates, 2 rows in flight per warp); other
+// instances run 16 warps.
 //
-// Phase 1 (the streaming part, bound by HBM and issue rate): every warp is its own row
-//   engine.  Its lane 0 keeps D rows in flight with one-dimensional bulk copies
-//   (cp.async.bulk, completion on a per-slot mbarrier) into a private ring in shared
-//   memory; the warp routes each row (route_row), writes packed ids coalesced, and
-//   counts the relabelled ids in its own 16-bit counters wcnt[w][bin].
-// Column pass: per bin, the 16 warp counters become 32-bit exclusive prefixes over
-//   warps (written over the ring, free by then) and their sum is the CTA's count,
-//   written to the expert-major matrix hist[bin][cta].
+// Phase 1 (the streaming part): every warp is its own row engine.  Its lane 0 keeps D
+//   rows in flight with one-dimensional bulk copies (cp.async.bulk, completion on a
+//   per-slot mbarrier) into a private ring in shared memory; the warp routes each row
+//   (route_row), writes packed ids coalesced, and counts the relabelled ids into the
+//   CTA's histogram, which goes to the expert-major matrix hist[bin][cta].
 // Grid barrier 1, then a column scan: for each bin one warp turns hist[bin][0..grid)
 //   into exclusive prefixes over CTAs and the bin's total.
 // Grid barrier 2, then phase 3: every CTA scans the totals into offsets (CTA 0 writes
-//   counts and offsets), adds its own CTA prefix, and every warp walks its rows in
-//   order: the entry (t, j) with relabelled id l goes to
+//   counts and offsets) and adds its own CTA prefix; each warp stages its packed ids in
+//   shared memory (the ring and scratch are free by then), counts its bins, a column
+//   pass over the warps turns the counts into warp prefixes, and each warp walks its
+//   rows in order: the entry (t, j) with relabelled id l goes to
 //   perm[offsets[l] + cta prefix + warp prefix + running count of l in this warp],
 //   which is its stable (id, token, slot) position, since ids are unique in a row.
-//   No block barrier inside the walk.
 // Every wait (mbarrier, grid barrier) is bounded in time; a wait that runs out sets
 // the device status word and the kernel returns.
 #include <cooperative_groups.h>
@@ -26,33 +26,42 @@
 
 namespace moe {
 
-constexpr int kPrefillWarps = 16;
-constexpr int kPrefillThreads = 32 * kPrefillWarps;
-
 __host__ __device__ constexpr int p_align(int x, int a) { return (x + a - 1) / a * a; }
 
-template <int DT>
+template <int DT, bool SPEC>
 struct PrefillSmem {
+  static constexpr bool WIDE = (DT == DT_BF16) && SPEC;
+  static constexpr int NW = WIDE ? 24 : 16;                  // warps per CTA
   static constexpr int ROWB = (DT == DT_BF16) ? kE * 2 : kE * 4;
-  static constexpr int D = (DT == DT_BF16) ? 3 : 2;  // rows in flight per warp
+  static constexpr int D = WIDE ? 2 : ((DT == DT_BF16) ? 3 : 2);  // rows in flight per warp
+  static constexpr int NB = SPEC ? 4 * kLanesPerGroup * kEPL : kEPL * 32;
+  using WS = WarpScratchT<NB>;
   static constexpr int STAB = (DT == DT_BF16) ? kSigTablePad * 4 : 0;
   static constexpr int o_stab = 0;
-  static constexpr int o_ring = p_align(o_stab + STAB, 128);
-  static constexpr int o_ws = p_align(o_ring + kPrefillWarps * D * ROWB, 128);
-  static constexpr int o_wcnt = p_align(o_ws + kPrefillWarps * int(sizeof(WarpScratch)), 128);
-  static constexpr int o_hist = p_align(o_wcnt + kPrefillWarps * kMaxBins * 2, 128);
+  static constexpr int o_bias = p_align(o_stab + STAB, 128);
+  static constexpr int o_ring = p_align(o_bias + kE * 4, 128);
+  static constexpr int o_ws = o_ring + NW * D * ROWB;         // 128-aligned: ROWB is
+  static constexpr int o_hist = p_align(o_ws + NW * int(sizeof(WS)), 128);
   static constexpr int o_base = p_align(o_hist + (kMaxBins + 1) * 4, 128);
   static constexpr int o_tmp = p_align(o_base + (kMaxBins + 1) * 4, 128);
   static constexpr int o_mbar = p_align(o_tmp + 33 * 4, 128);
-  static constexpr int total = o_mbar + kPrefillWarps * D * 8 + 64;
+  static constexpr int total = o_mbar + NW * D * 8 + 64;
+  // phase 3 reuses [o_ring, o_hist): warp prefixes, then a staging buffer per warp
+  static constexpr int REGION = o_hist - o_ring;
+  static constexpr int STAGE_INTS = (REGION / 4 - NW * kMaxBins) / NW;
 };
 
-static_assert(PrefillSmem<DT_F32>::total <= 227 * 1024, "prefill smem (f32) exceeds 227 KB");
-static_assert(PrefillSmem<DT_BF16>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
-static_assert(kMaxBins % 2 == 0, "16-bit counters are updated in 32-bit pairs");
-static_assert(PrefillSmem<DT_BF16>::D * PrefillSmem<DT_BF16>::ROWB >= kMaxBins * 4 &&
-                  PrefillSmem<DT_F32>::D * PrefillSmem<DT_F32>::ROWB >= kMaxBins * 4,
-              "32-bit warp prefixes reuse the ring");
+static_assert(PrefillSmem<DT_F32, false>::total <= 227 * 1024, "prefill smem (f32) exceeds 227 KB");
+static_assert(PrefillSmem<DT_F32, true>::total <= 227 * 1024, "prefill smem (f32) exceeds 227 KB");
+static_assert(PrefillSmem<DT_BF16, false>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
+static_assert(PrefillSmem<DT_BF16, true>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
+static_assert(PrefillSmem<DT_BF16, true>::STAGE_INTS >= 4 * kMaxK &&
+                  PrefillSmem<DT_BF16, false>::STAGE_INTS >= 4 * kMaxK &&
+                  PrefillSmem<DT_F32, true>::STAGE_INTS >= 4 * kMaxK &&
+                  PrefillSmem<DT_F32, false>::STAGE_INTS >= 4 * kMaxK,
+              "phase 3 needs room for a few staged rows per warp");
+static_assert(PrefillSmem<DT_BF16, true>::ROWB % 128 == 0 && PrefillSmem<DT_F32, true>::ROWB % 128 == 0,
+              "row slots keep 128-byte alignment");
 
 // Grid-wide barrier for a cooperative launch, bounded in time.  One arrival counter:
 // CTA 0 adds 2^31 - (nblocks - 1), every other CTA adds 1, so the counter's top bit
@@ -127,15 +136,19 @@ __device__ __forceinline__ void block_scan_fast(const int* in, int* out, int n, 
 }
 
 // SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).
+// SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).
 template <int DT, bool SPEC>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+__global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
     k_route_prefill(RouteArgs a, PrefillWS pw) {
-  using L = PrefillSmem<DT>;
+  using L = PrefillSmem<DT, SPEC>;
+  using WS = typename L::WS;
+  constexpr int NW = L::NW;
+  constexpr int NT = NW * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   float* stab = reinterpret_cast<float*>(smem + L::o_stab);
+  float* bias_s = reinterpret_cast<float*>(smem + L::o_bias);
   uint8_t* ring_all = smem + L::o_ring;
-  WarpScratch* wsp = reinterpret_cast<WarpScratch*>(smem + L::o_ws);
-  uint16_t* wcnt_all = reinterpret_cast<uint16_t*>(smem + L::o_wcnt);
+  WS* wsp = reinterpret_cast<WS*>(smem + L::o_ws);
   int* hist_s = reinterpret_cast<int*>(smem + L::o_hist);
   int* base_s = reinterpret_cast<int*>(smem + L::o_base);
   int* tmp = reinterpret_cast<int*>(smem + L::o_tmp);
@@ -146,31 +159,30 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int r0 = int((long long)a.T * cta / grid);
   const int r1 = int((long long)a.T * (cta + 1) / grid);
   // this warp's rows: [wr0, wr1)
-  const int per_warp = (r1 - r0 + kPrefillWarps - 1) / kPrefillWarps;
+  const int per_warp = (r1 - r0 + NW - 1) / NW;
   const int wr0 = min(r1, r0 + w * per_warp);
   const int wr1 = min(r1, wr0 + per_warp);
   const int nw = wr1 - wr0;
   uint8_t* ring = ring_all + w * L::D * L::ROWB;
   uint64_t* mb = mbar_all + w * L::D;
-  uint16_t* wcnt = wcnt_all + w * kMaxBins;
-  uint32_t* wcnt32 = reinterpret_cast<uint32_t*>(wcnt);
   const uint8_t* logits = static_cast<const uint8_t*>(a.logits);
 
-  // ---- setup: mbarriers, counters, sigmoid table, first rows in flight
+  // ---- setup: mbarriers, histogram, score table and bias, first rows in flight
   if (lane == 0) {
     for (int d = 0; d < L::D; ++d) mbar_init(mb + d, 1);
     fence_mbar_init();
   }
-  uint64_t* tab_bar = mbar_all + kPrefillWarps * L::D;
-  if (tid == 0 && L::STAB) {
+  uint64_t* tab_bar = mbar_all + NW * L::D;
+  if (tid == 0) {
     mbar_init(tab_bar, 1);
     fence_mbar_init();
   }
-  for (int e = lane; e < (a.NE + 1) / 2; e += 32) wcnt32[e] = 0u;
+  for (int e = tid; e < a.NE; e += NT) hist_s[e] = 0;
   __syncthreads();
-  if (tid == 0 && L::STAB) {
-    mbar_expect_tx(tab_bar, L::STAB);
-    bulk_g2s(stab, a.stab, L::STAB, tab_bar);
+  if (tid == 0) {
+    mbar_expect_tx(tab_bar, uint32_t(L::STAB + kE * 4));
+    if (L::STAB) bulk_g2s(stab, a.stab, L::STAB, tab_bar);
+    bulk_g2s(bias_s, a.bias, kE * 4, tab_bar);
   }
   if (lane == 0) {
     for (int d = 0; d < L::D && d < nw; ++d) {
@@ -178,9 +190,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       bulk_g2s(ring + d * L::ROWB, logits + size_t(wr0 + d) * L::ROWB, L::ROWB, mb + d);
     }
   }
-  float bl[kEPL];
-  load_lane_bias(a.bias, bl);
-  if (L::STAB) mbar_wait_bounded(tab_bar, 0, a.err);
+  mbar_wait_bounded(tab_bar, 0, a.err);
 
   // ---- phase 1: route this warp's rows
   for (int i = 0; i < nw; ++i) {
@@ -189,12 +199,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     mbar_wait_bounded(mb + slot, par, a.err);
     const int t = wr0 + i;
     const SlotOut o =
-        route_row<DT, SPEC ? 16 : 0, SPEC ? 4 : 0>(ring + slot * L::ROWB, bl, stab, a, wsp[w]);
+        route_row<DT, SPEC ? 16 : 0, SPEC ? 4 : 0>(ring + slot * L::ROWB, bias_s, stab, a, wsp[w]);
     if (lane < a.k) {
       a.packed[size_t(t) * a.k + lane] = o.packed;
       if (a.ids) a.ids[size_t(t) * a.k + lane] = o.id;
-      // ids are unique in a row; two lanes may share a 32-bit word (bins 2m, 2m+1)
-      atomicAdd(&wcnt32[o.lid >> 1], 1u << ((o.lid & 1) * 16));
+      atomicAdd(&hist_s[o.lid], 1);
     }
     __syncwarp();
     if (lane == 0 && i + L::D < nw) {
@@ -204,27 +213,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     }
   }
   __syncthreads();
-
-  // ---- column pass: warp prefixes per bin (32-bit, over the ring: every bulk copy into
-  //      it has completed), CTA count per bin
-  int* wpre_all = reinterpret_cast<int*>(ring_all);
-  for (int e = tid; e < a.NE; e += kPrefillThreads) {
-    int run = 0;
-#pragma unroll
-    for (int w2 = 0; w2 < kPrefillWarps; ++w2) {
-      const int v = wcnt_all[w2 * kMaxBins + e];
-      wpre_all[w2 * kMaxBins + e] = run;
-      run += v;
-    }
-    pw.hist[size_t(e) * pw.grid_max + cta] = run;
-  }
+  for (int e = tid; e < a.NE; e += NT) pw.hist[size_t(e) * pw.grid_max + cta] = hist_s[e];
 
   int* flag_s = tmp + 32;
   if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
 
   // ---- column scan over CTAs, one warp per bin; lane l covers up to 8 consecutive CTAs
   //      per pass of 256
-  for (int e = cta * kPrefillWarps + w; e < a.NE; e += grid * kPrefillWarps) {
+  for (int e = cta * NW + w; e < a.NE; e += grid * NW) {
     const int* h = pw.hist + size_t(e) * pw.grid_max;
     int* p = pw.prefix + size_t(e) * pw.grid_max;
     int carry = 0;
@@ -259,29 +255,29 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
 
   // ---- phase 3: offsets, then this CTA's permutation entries
-  for (int e = tid; e < a.NE; e += kPrefillThreads) hist_s[e] = __ldcg(pw.counts + e);
+  for (int e = tid; e < a.NE; e += NT) hist_s[e] = __ldcg(pw.counts + e);
   __syncthreads();
   block_scan_fast(hist_s, base_s, a.NE, tmp);
   if (cta == 0) {
-    for (int e = tid; e < a.NE; e += kPrefillThreads) {
+    for (int e = tid; e < a.NE; e += NT) {
       a.counts[e] = hist_s[e];
       a.offsets[e] = base_s[e];
     }
     if (tid == 0) a.offsets[a.NE] = base_s[a.NE];
   }
-  for (int e = tid; e < a.NE; e += kPrefillThreads) base_s[e] += __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
-  __syncthreads();
-  // The walk: this warp's packed ids are staged in its (now free) routing scratch, a
-  // chunk of rows at a time, with all loads of a chunk in flight at once; the rows are
-  // then taken in order from shared memory.
+  for (int e = tid; e < a.NE; e += NT) base_s[e] += __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
+
+  // The ring and the routing scratch are free: warp counters [NW][kMaxBins], then a
+  // staging buffer per warp for its packed ids, loaded a chunk of rows at a time with
+  // all loads of a chunk in flight.
+  int* wpre_all = reinterpret_cast<int*>(ring_all);
   int* wpre = wpre_all + w * kMaxBins;
-  int* stage = reinterpret_cast<int*>(wsp + w);
-  constexpr int kStageInts = int(sizeof(WarpScratch)) / 4;
-  const int chunk_rows = kStageInts / a.k;
+  int* stage = wpre_all + NW * kMaxBins + w * L::STAGE_INTS;
+  const int chunk_rows = L::STAGE_INTS / a.k;
+  const int nchunks = (nw + chunk_rows - 1) / chunk_rows;
   const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
-  for (int c0 = 0; c0 < nw; c0 += chunk_rows) {
-    const int nr = min(chunk_rows, nw - c0);
-    const int n = nr * a.k;
+  auto stage_chunk = [&](int c0) {
+    const int n = min(chunk_rows, nw - c0) * a.k;
     const int32_t* src = a.packed + size_t(wr0 + c0) * a.k;
     for (int i0 = 0; i0 < n; i0 += 8 * 32) {
       int32_t v[8];
@@ -297,6 +293,34 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
     }
     __syncwarp();
+  };
+  __syncthreads();  // every warp is done with the ring and its scratch
+  for (int e = lane; e < a.NE; e += 32) wpre[e] = 0;
+  __syncwarp();
+  // this warp's bin counts
+  for (int c0 = 0; c0 < nw; c0 += chunk_rows) {
+    stage_chunk(c0);
+    const int nr = min(chunk_rows, nw - c0);
+    if (lane < a.k)
+      for (int r = 0; r < nr; ++r) atomicAdd(&wpre[int(uint32_t(stage[r * a.k + lane]) >> 16)], 1);
+    __syncwarp();
+  }
+  __syncthreads();
+  // warp prefixes per bin
+  for (int e = tid; e < a.NE; e += NT) {
+    int run = 0;
+#pragma unroll 4
+    for (int w2 = 0; w2 < NW; ++w2) {
+      const int v = wpre_all[w2 * kMaxBins + e];
+      wpre_all[w2 * kMaxBins + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // the walk: rows in order (the last chunk staged above is still in place)
+  for (int c0 = 0; c0 < nw; c0 += chunk_rows) {
+    if (nchunks > 1) stage_chunk(c0);
+    const int nr = min(chunk_rows, nw - c0);
     if (lane < a.k) {
       for (int r = 0; r < nr; ++r) {
         const int l = int(uint32_t(stage[r * a.k + lane]) >> 16);
@@ -314,11 +338,12 @@ template <int DT, bool SPEC>
 static cudaError_t set_prefill_smem(int* bmin) {
   cudaError_t e = cudaFuncSetAttribute(k_route_prefill<DT, SPEC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PrefillSmem<DT>::total);
+                                       PrefillSmem<DT, SPEC>::total);
   if (e != cudaSuccess) return e;
   int b = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_route_prefill<DT, SPEC>, kPrefillThreads,
-                                                    PrefillSmem<DT>::total);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_route_prefill<DT, SPEC>,
+                                                    PrefillSmem<DT, SPEC>::NW * 32,
+                                                    PrefillSmem<DT, SPEC>::total);
   if (e != cudaSuccess) return e;
   *bmin = min(*bmin, b);
   return cudaSuccess;
@@ -335,34 +360,30 @@ cudaError_t setup_prefill_kernels(int* blocks_per_sm) {
   return cudaSuccess;
 }
 
-bool prefill_fits(int T, int grid) {
-  // per-warp 16-bit counters: a warp's rows must stay below 65,536
-  if (grid < 1) return false;
-  const long long rows_cta = (static_cast<long long>(T) + grid - 1) / grid;
-  return (rows_cta + kPrefillWarps - 1) / kPrefillWarps < 65536;
-}
+bool prefill_fits(int T, int grid) { return T >= 0 && grid >= 1; }
 
-cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,
-                                 cudaStream_t st) {
-  if (!prefill_fits(a.T, grid)) return cudaErrorInvalidValue;
+template <int DT, bool SPEC>
+static cudaError_t launch_t(const RouteArgs& a, const PrefillWS& ws, int grid, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kPrefillThreads, 1, 1);
+  cfg.blockDim = dim3(PrefillSmem<DT, SPEC>::NW * 32, 1, 1);
+  cfg.dynamicSmemBytes = PrefillSmem<DT, SPEC>::total;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_route_prefill<DT, SPEC>, a, ws);
+}
+
+cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,
+                                 cudaStream_t st) {
+  if (!prefill_fits(a.T, grid)) return cudaErrorInvalidValue;
   const bool spec = a.k == 16 && a.Kg == 4;
-  if (dtype == DT_BF16) {
-    cfg.dynamicSmemBytes = PrefillSmem<DT_BF16>::total;
-    return spec ? cudaLaunchKernelEx(&cfg, k_route_prefill<DT_BF16, true>, a, ws)
-                : cudaLaunchKernelEx(&cfg, k_route_prefill<DT_BF16, false>, a, ws);
-  }
-  cfg.dynamicSmemBytes = PrefillSmem<DT_F32>::total;
-  return spec ? cudaLaunchKernelEx(&cfg, k_route_prefill<DT_F32, true>, a, ws)
-              : cudaLaunchKernelEx(&cfg, k_route_prefill<DT_F32, false>, a, ws);
+  if (dtype == DT_BF16)
+    return spec ? launch_t<DT_BF16, true>(a, ws, grid, st) : launch_t<DT_BF16, false>(a, ws, grid, st);
+  return spec ? launch_t<DT_F32, true>(a, ws, grid, st) : launch_t<DT_F32, false>(a, ws, grid, st);
 }
 
 }  // namespace moe

@@ -37,14 +37,17 @@ struct RouteArgs {
   float scale;
 };
 
-// Per-warp shared scratch of the row routine.
-struct WarpScratch {
-  float b[kEPL * 32];     // biased scores of the kept lanes (kept lane i at [28 i, 28 i + 28))
+// Per-warp shared scratch of the row routine.  NB = biased scores parked by the kept
+// lanes: 28 per kept lane (448 when 4 of the 8 groups are kept, 896 at most).
+template <int NB>
+struct WarpScratchT {
+  float b[NB];            // biased scores of the kept lanes (kept lane i at [28 i, 28 i + 28))
   float pool[32];         // threshold pool
   uint32_t skey[32];      // survivor keys
   int32_t sid[32];        // survivor expert ids
   int32_t slot_id[kMaxK]; // expert id of each slot
 };
+using WarpScratch = WarpScratchT<kEPL * 32>;
 
 // Row input kinds: float32 logits, bfloat16 logits, or float32 scores already equal to
 // sigmoid(logit) (the fused contraction computes them in its epilogue).
@@ -62,19 +65,6 @@ __device__ __forceinline__ float row_sigmoid(const void* row, int e, const float
   }
 }
 
-// Loads this lane's 28 biases into registers.
-__device__ __forceinline__ void load_lane_bias(const float* __restrict__ bias, float (&bl)[kEPL]) {
-  const int lane = threadIdx.x & 31;
-  const float4* p = reinterpret_cast<const float4*>(bias + lane * kEPL);
-#pragma unroll
-  for (int q = 0; q < kEPL / 4; ++q) {
-    const float4 v = __ldg(p + q);
-    bl[4 * q + 0] = v.x;
-    bl[4 * q + 1] = v.y;
-    bl[4 * q + 2] = v.z;
-    bl[4 * q + 3] = v.w;
-  }
-}
 
 // Result of one routed row, valid in lanes j < k.
 struct SlotOut {
@@ -118,12 +108,12 @@ __device__ __forceinline__ void sig_bf16_pair(const float* tab_lo, uint32_t v, f
 }
 
 // Routes one row.  `row` points to the row's E logits (or scores) in shared memory
-// (16-byte aligned).  All 32 lanes must call it.  KC and KGC fix k and topk_group at
-// compile time (the Kimi-K3 instance: 16 and 4); 0 reads them from `a`.
-template <int DT, int KC = 0, int KGC = 0>
-__device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[kEPL],
-                                             const float* stab, const RouteArgs& a,
-                                             WarpScratch& ws) {
+// (16-byte aligned); `bias_s` to the E biases in shared memory (16-byte aligned).  All
+// 32 lanes must call it.  KC and KGC fix k and topk_group at compile time (the Kimi-K3
+// instance: 16 and 4); 0 reads them from `a`.
+template <int DT, int KC = 0, int KGC = 0, class WS>
+__device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_s,
+                                             const float* stab, const RouteArgs& a, WS& ws) {
   const unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int e0 = lane * kEPL;
@@ -131,6 +121,7 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
   const int Kg = KGC ? KGC : a.Kg;
 
   // ---- a1, a2: scores, biased scores, lane top-2 (two independent lists)
+  const float4* bq = reinterpret_cast<const float4*>(bias_s + e0);
   float b[kEPL];
   float xa1 = -INFINITY, xa2 = -INFINITY, xb1 = -INFINITY, xb2 = -INFINITY;
   if constexpr (DT == DT_BF16) {
@@ -139,13 +130,14 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
 #pragma unroll
     for (int q = 0; q < kEPL / 4; ++q) {
       const uint2 v = p[q];
+      const float4 bb = bq[q];
       float s0, s1, s2, s3;
       sig_bf16_pair(tab_lo, v.x, s0, s1);
       sig_bf16_pair(tab_lo, v.y, s2, s3);
-      b[4 * q + 0] = __fadd_rn(s0, bl[4 * q + 0]);
-      b[4 * q + 1] = __fadd_rn(s1, bl[4 * q + 1]);
-      b[4 * q + 2] = __fadd_rn(s2, bl[4 * q + 2]);
-      b[4 * q + 3] = __fadd_rn(s3, bl[4 * q + 3]);
+      b[4 * q + 0] = __fadd_rn(s0, bb.x);
+      b[4 * q + 1] = __fadd_rn(s1, bb.y);
+      b[4 * q + 2] = __fadd_rn(s2, bb.z);
+      b[4 * q + 3] = __fadd_rn(s3, bb.w);
       top2_pair(xa1, xa2, b[4 * q + 0], b[4 * q + 1]);
       top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
     }
@@ -154,11 +146,13 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float (&bl)[
 #pragma unroll
     for (int q = 0; q < kEPL / 4; ++q) {
       const float4 v = p[q];
+      const float4 bb = bq[q];
       const float x[4] = {v.x, v.y, v.z, v.w};
+      const float bi[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const float sc = (DT == DT_SCORE) ? x[r] : sig_f32(x[r], a.etab);
-        b[4 * q + r] = __fadd_rn(sc, bl[4 * q + r]);
+        b[4 * q + r] = __fadd_rn(sc, bi[r]);
       }
       top2_pair(xa1, xa2, b[4 * q + 0], b[4 * q + 1]);
       top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
