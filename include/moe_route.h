@@ -40,8 +40,7 @@
  *     an error has enqueued nothing.  Errors detected on the device (a bounded wait
  *     that ran out) are reported by moe_route_device_status().
  *   - Supported shapes: E = 896 with n_group = 8 (the Kimi-K3 grouping), any
- *     topk_group in [1, 8], 1 <= k <= 32 with k <= topk_group * 112, and T up to
- *     about 65,535 * 16 rows per SM (about 159 M rows on 152 SMs).  Other valid
+ *     topk_group in [1, 8], 1 <= k <= 32 with k <= topk_group * 112.  Other valid
  *     shapes return MOE_ROUTE_E_UNSUPPORTED.
  */
 #ifndef MOE_ROUTE_H
