@@ -109,16 +109,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   __syncthreads();
   if (tid == 0 && have) {
     mbar_expect_tx(mbar, bytes);
+    // the score table is the library's own constant: it may be read before the
+    // preceding kernel completes
     if (L::STAB) bulk_g2s(stab, a.stab, L::STAB, mbar);
-    bulk_g2s(bias_s, a.bias, kE * 4, mbar);
-    bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
-             uint32_t(nrows) * L::ROWB, mbar);
   }
   // every CTA of the cluster must be running before another one stores into its shared
   // memory: arrive now (relaxed: nothing to publish, and no wait for the copies in
   // flight), wait after routing
   for (int e = tid; e < a.NE; e += kDecodeThreads) mask_s[e] = 0ull;
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  // launched as a programmatic dependent: everything above overlaps the preceding
+  // kernel; inputs are read and outputs written only after it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0 && have) {
+    bulk_g2s(bias_s, a.bias, kE * 4, mbar);
+    bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
+             uint32_t(nrows) * L::ROWB, mbar);
+  }
   if (have) mbar_wait_bounded(mbar, 0, a.err);
 
   SlotOut o = {};
@@ -263,13 +270,15 @@ cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) 
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ctas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   const bool spec = a.k == 16 && a.Kg == 4;
   if (dtype == DT_BF16) return spec ? launch_decode_t<DT_BF16, true>(cfg, a) : launch_decode_t<DT_BF16, false>(cfg, a);
   if (dtype == DT_SCORE) return spec ? launch_decode_t<DT_SCORE, true>(cfg, a) : launch_decode_t<DT_SCORE, false>(cfg, a);

@@ -36,7 +36,7 @@ constexpr int kStageH = 64 * kBK * 2;  // room for N <= 64 token rows: 8 KB
 constexpr int kStage = kStageW + kStageH;
 constexpr int kMaxStages = 7;
 constexpr int kTmemCols = 64;
-constexpr int kRowPad = 64 + 4;       // padded row of 64 token partial sums (conflict-free)
+constexpr int kRowPad = 64 + 4;       // longest staging row: 64 token partial sums + padding
 constexpr int kRecvBytes = kBM * kRowPad * 4;  // receive buffer: C sources x (128/C) rows
 
 struct GemmArgs {
@@ -100,8 +100,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                   GemmArgs g) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled stages
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
+  // (offset from the shared array itself, so the compiler keeps shared-memory accesses)
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   cg::cluster_group cluster = cg::this_cluster();
   const int C = static_cast<int>(cluster.num_blocks());
   const int r = static_cast<int>(cluster.block_rank());
@@ -109,6 +109,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int mtile = blockIdx.x / C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = g.stages;
+  // the routing kernel that reads this kernel's scores may launch now; it waits for
+  // this grid's completion (griddepcontrol.wait) before it reads them
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   uint8_t* stages = smem;
   float* recv = reinterpret_cast<float*>(smem + kMaxStages * kStage);  // [C][R][kRowPad]
@@ -120,7 +123,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   float* stage_rows = reinterpret_cast<float*>(stages);  // [128][kRowPad], reuses the ring
   const int kb0 = r * g.kb_per_cta;
   const uint32_t stage_bytes = uint32_t(kStageW + g.Tpad * kBK * 2);
-  const uint32_t copy_bytes = uint32_t(R * kRowPad * 4);
+  // staging and receive rows hold Tpad token sums (+4 floats of padding)
+  const int rs = g.Tpad + 4;
+  const uint32_t copy_bytes = uint32_t(R * rs * 4);
 
   if (threadIdx.x == 0) {
     // barriers, then every stage's loads at once (the ring holds the whole K slice when
@@ -212,11 +217,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         : "r"(ta)
         : "memory");
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    float4* d4 = reinterpret_cast<float4*>(stage_rows + (warp * 32 + lane) * kRowPad);
+    float4* d4 = reinterpret_cast<float4*>(stage_rows + (warp * 32 + lane) * rs);
 #pragma unroll
     for (int c = 0; c < 16; ++c)
-      d4[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                          __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+      if (4 * c < g.Tpad)
+        d4[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                            __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
   }
   fence_proxy_async_smem();  // staging rows visible to the bulk-copy engine
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -227,8 +233,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     // rows [o R, o R + R) go to CTA o, into its receive slot for source r
     for (int o = 0; o < C; ++o) {
-      const uint32_t src = smem_addr(stage_rows + o * R * kRowPad);
-      const uint32_t dst = mapa_cluster(smem_addr(recv + r * R * kRowPad), o);
+      const uint32_t src = smem_addr(stage_rows + o * R * rs);
+      const uint32_t dst = mapa_cluster(smem_addr(recv + r * R * rs), o);
       const uint32_t bar = mapa_cluster(smem_addr(recv_bar), o);
       asm volatile(
           "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       for (int c = 0; c < C; ++c) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], recv[(c * R + i0 + q) * kRowPad + t]);
+        for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], recv[(c * R + i0 + q) * rs + t]);
       }
       const int e = mtile * kBM + r * R + i0;
       if (g.logits)
