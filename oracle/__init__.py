@@ -62,6 +62,12 @@ def _bind(lib):
     lib.oracle_router_gemm.restype = None
     lib.oracle_route_layout.argtypes = [P, P, P, I, I, I, I, P, P, P, P]
     lib.oracle_route_layout.restype = I
+    lib.oracle_route_index.argtypes = [P, I, I, I, P, P, P]
+    lib.oracle_route_index.restype = I
+    lib.oracle_dispatch_counts.argtypes = [P, I, I, I, P, P]
+    lib.oracle_dispatch_counts.restype = I
+    lib.oracle_alltoall_layout.argtypes = [P, I, I, P, P, P]
+    lib.oracle_alltoall_layout.restype = I
     return lib
 
 
@@ -145,3 +151,41 @@ def route_layout(counts: np.ndarray, offsets: np.ndarray, perm: np.ndarray, tile
     if total < 0:
         raise ValueError("oracle_route_layout rejected its arguments")
     return dict(inv_perm=inv, padded_offsets=poff, padded_rows=rows, m_indices=mind, total=total)
+
+
+def route_index(packed: np.ndarray, NE: int, lib=None) -> dict:
+    """counts, offsets and perm of packed values [T, k] (steps 10-12 alone)."""
+    packed = np.ascontiguousarray(packed, dtype=np.int32)
+    T, k = packed.shape
+    counts = np.empty(NE, np.int32)
+    offsets = np.empty(NE + 1, np.int32)
+    perm = np.empty(T * k, np.int32)
+    rc = (lib or load()).oracle_route_index(_ptr(packed), T, k, NE, _ptr(counts), _ptr(offsets),
+                                            _ptr(perm))
+    if rc != 0:
+        raise ValueError("oracle_route_index rejected its arguments")
+    return dict(counts=counts, offsets=offsets, perm=perm)
+
+
+def dispatch_counts(ids: np.ndarray, E: int, R: int, lib=None) -> dict:
+    """Entries per destination rank for global expert ids (R ranks, E / R experts each)."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32).ravel()
+    sc = np.empty(R, np.int32)
+    so = np.empty(R + 1, np.int32)
+    rc = (lib or load()).oracle_dispatch_counts(_ptr(ids), ids.size, E, R, _ptr(sc), _ptr(so))
+    if rc != 0:
+        raise ValueError("oracle_dispatch_counts rejected its arguments")
+    return dict(send_counts=sc, send_offsets=so)
+
+
+def alltoall_layout(matrix: np.ndarray, me: int, lib=None) -> dict:
+    """send displacements, receive counts and displacements of rank `me`."""
+    m = np.ascontiguousarray(matrix, dtype=np.int32)
+    R = m.shape[0]
+    sd = np.empty(R + 1, np.int32)
+    rcnt = np.empty(R, np.int32)
+    rd = np.empty(R + 1, np.int32)
+    rc = (lib or load()).oracle_alltoall_layout(_ptr(m), R, me, _ptr(sd), _ptr(rcnt), _ptr(rd))
+    if rc != 0:
+        raise ValueError("oracle_alltoall_layout rejected its arguments")
+    return dict(send_displs=sd, recv_counts=rcnt, recv_displs=rd)

@@ -239,3 +239,54 @@ int oracle_route_layout(const int32_t* counts, const int32_t* offsets, const int
     free(poff);
     return (int)total;
 }
+
+int oracle_route_index(const int32_t* packed, int T, int k, int NE, int32_t* counts,
+                       int32_t* offsets, int32_t* perm) {
+    if (T < 0 || k < 1 || NE < 1) return -1;
+    size_t n = (size_t)T * k;
+    for (size_t i = 0; i < n; ++i)
+        if ((int)((uint32_t)packed[i] >> 16) >= NE) return -1;
+    /* histogram of the ids in the packed values */
+    for (int e = 0; e < NE; ++e) counts[e] = 0;
+    for (size_t i = 0; i < n; ++i) counts[(uint32_t)packed[i] >> 16] += 1;
+    /* exclusive scan */
+    offsets[0] = 0;
+    for (int e = 0; e < NE; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    /* stable permutation ordered by (id, token, slot) */
+    int32_t* cursor = (int32_t*)malloc(sizeof(int32_t) * (size_t)NE);
+    for (int e = 0; e < NE; ++e) cursor[e] = offsets[e];
+    for (size_t i = 0; i < n; ++i) {
+        int l = (int)((uint32_t)packed[i] >> 16);
+        perm[cursor[l]] = (int32_t)i;
+        cursor[l] += 1;
+    }
+    free(cursor);
+    return 0;
+}
+
+int oracle_dispatch_counts(const int32_t* ids, int n, int E, int R, int32_t* send_counts,
+                           int32_t* send_offsets) {
+    if (n < 0 || E < 1 || R < 1 || E % R != 0) return -1;
+    int per = E / R;
+    for (int d = 0; d < R; ++d) send_counts[d] = 0;
+    for (int i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= E) return -1;
+        send_counts[ids[i] / per] += 1;
+    }
+    send_offsets[0] = 0;
+    for (int d = 0; d < R; ++d) send_offsets[d + 1] = send_offsets[d] + send_counts[d];
+    return 0;
+}
+
+int oracle_alltoall_layout(const int32_t* matrix, int R, int me, int32_t* send_displs,
+                           int32_t* recv_counts, int32_t* recv_displs) {
+    if (R < 1 || me < 0 || me >= R) return -1;
+    send_displs[0] = 0;
+    for (int d = 0; d < R; ++d) send_displs[d + 1] = send_displs[d] + matrix[(size_t)me * R + d];
+    recv_displs[0] = 0;
+    for (int s = 0; s < R; ++s) {
+        recv_counts[s] = matrix[(size_t)s * R + me];
+        recv_displs[s + 1] = recv_displs[s] + recv_counts[s];
+    }
+    return 0;
+}

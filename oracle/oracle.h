@@ -86,6 +86,28 @@ int oracle_route_layout(const int32_t* counts, const int32_t* offsets, const int
                         int NE, int tile, int capacity, int32_t* inv_perm, int32_t* padded_offsets,
                         int32_t* padded_rows, int32_t* m_indices);
 
+/* Steps 10-12 alone, from packed values (id << 16 | weight) of T rows of k slots, as
+ * gathered from token-sharded routing (each rank routes a contiguous slice of the tokens
+ * and the top-k results are gathered -- vLLM PR #59693, description of the sharded
+ * path): counts [NE], offsets [NE + 1], perm [T * k] exactly as oracle_route defines
+ * them.  Returns 0, or -1 for invalid arguments or an id >= NE. */
+int oracle_route_index(const int32_t* packed, int T, int k, int NE, int32_t* counts,
+                       int32_t* offsets, int32_t* perm);
+
+/* Expert-parallel dispatch layout (vLLM PR #54606, description: a variable-size
+ * all-to-all driven by a counts matrix).  R ranks own contiguous expert ranges of
+ * E / R experts; for n global expert ids, send_counts[d] = entries whose expert rank d
+ * owns, send_offsets = exclusive scan (R + 1).  Returns 0, or -1 for invalid arguments
+ * (E % R != 0, an id outside [0, E)). */
+int oracle_dispatch_counts(const int32_t* ids, int n, int E, int R, int32_t* send_counts,
+                           int32_t* send_offsets);
+
+/* All-to-all layout of rank `me` from the gathered counts matrix [R][R] (row = source,
+ * column = destination): send_displs = exclusive scan of row me (R + 1), recv_counts =
+ * column me, recv_displs = its exclusive scan (R + 1).  Returns 0 or -1. */
+int oracle_alltoall_layout(const int32_t* matrix, int R, int me, int32_t* send_displs,
+                           int32_t* recv_counts, int32_t* recv_displs);
+
 #ifdef __cplusplus
 }
 #endif

@@ -479,10 +479,93 @@ def pin_layout_rejects(lib):
         raise AssertionError(f"layout accepted tile={tile} capacity={cap}")
 
 
+def pin_route_index(lib):
+    """Histogram, scan and stable permutation from packed values alone: numpy bincount,
+    cumsum and stable argsort of the ids, for routing outputs and for arbitrary packed
+    arrays (repeated ids in a row included); ids >= NE are rejected."""
+    for cfg in (gen.cfg1(24), gen.cfg1(64, off=0, cnt=0), gen.cfg4(T=200, n_hot=50, off=336, cnt=112)):
+        out = run(lib, cfg)
+        r = oracle.route_index(out["packed"], out["NE"], lib=lib)
+        for key in ("counts", "offsets", "perm"):
+            assert np.array_equal(r[key], out[key]), key
+    for seed, (T, k, NE) in enumerate(((1, 1, 1), (7, 3, 5), (50, 16, 128), (33, 8, 1056))):
+        ids = (gen.raw64(3000 + seed, T * k) % np.uint64(NE)).astype(np.int64)
+        packed = ((ids << 16) | 0x3E20).astype(np.int32).reshape(T, k)
+        r = oracle.route_index(packed, NE, lib=lib)
+        assert np.array_equal(r["counts"], np.bincount(ids, minlength=NE))
+        assert np.array_equal(r["offsets"], np.concatenate([[0], np.cumsum(np.bincount(ids, minlength=NE))]))
+        assert np.array_equal(r["perm"], np.argsort(ids, kind="stable"))
+    bad = np.array([[5 << 16]], dtype=np.int32)
+    try:
+        oracle.route_index(bad, 5, lib=lib)
+    except ValueError:
+        return
+    raise AssertionError("route_index accepted an id >= NE")
+
+
+def pin_token_sharded(lib):
+    """Rows are independent: routing contiguous token shards and gathering their packed
+    values gives the full batch's packed values, and the index built from the gathered
+    values is the full batch's counts, offsets and perm."""
+    cfg = gen.cfg3(1000, off=784, cnt=112)
+    full = run(lib, cfg)
+    for R in (2, 3, 8):
+        parts = []
+        for r in range(R):
+            lo, hi = 1000 * r // R, 1000 * (r + 1) // R
+            sub = dict(cfg, logits=cfg["logits"][lo:hi], T=hi - lo)
+            parts.append(run(lib, sub)["packed"])
+        gathered = np.concatenate(parts)
+        assert np.array_equal(gathered, full["packed"])
+        r = oracle.route_index(gathered, full["NE"], lib=lib)
+        for key in ("counts", "offsets", "perm"):
+            assert np.array_equal(r[key], full[key]), (R, key)
+
+
+def pin_dispatch_counts(lib):
+    """Entries per destination rank = numpy bincount of id // (E / R); offsets = cumsum;
+    with global-id routing they are the expert offsets sampled at the rank boundaries."""
+    out = run(lib, gen.cfg3(500))
+    ids = out["ids"].ravel()
+    for R in (1, 2, 4, 7, 8, 16):
+        d = oracle.dispatch_counts(ids, 896, R, lib=lib)
+        ref = np.bincount(ids // (896 // R), minlength=R)
+        assert np.array_equal(d["send_counts"], ref)
+        assert np.array_equal(d["send_offsets"], np.concatenate([[0], np.cumsum(ref)]))
+        assert np.array_equal(d["send_offsets"], out["offsets"][np.arange(R + 1) * (896 // R)])
+    for bad in ((ids, 896, 5), (np.array([896]), 896, 8)):
+        try:
+            oracle.dispatch_counts(*bad, lib=lib)
+        except ValueError:
+            continue
+        raise AssertionError(f"dispatch_counts accepted {bad[1:]}")
+
+
+def pin_alltoall_layout(lib):
+    """A hand-worked 3-rank case; numpy cumsum of the matrix row and column; what rank s
+    sends to rank d is what rank d expects from rank s, for every pair."""
+    m = np.arange(9, dtype=np.int32).reshape(3, 3)
+    L = oracle.alltoall_layout(m, 1, lib=lib)
+    assert L["send_displs"].tolist() == [0, 3, 7, 12]
+    assert L["recv_counts"].tolist() == [1, 4, 7]
+    assert L["recv_displs"].tolist() == [0, 1, 5, 12]
+    R = 8
+    m = (gen.raw64(3100, R * R) % np.uint64(1000)).astype(np.int32).reshape(R, R)
+    lay = [oracle.alltoall_layout(m, me, lib=lib) for me in range(R)]
+    for me in range(R):
+        assert np.array_equal(lay[me]["send_displs"], np.concatenate([[0], np.cumsum(m[me])]))
+        assert np.array_equal(lay[me]["recv_displs"], np.concatenate([[0], np.cumsum(m[:, me])]))
+        for d in range(R):
+            sent = lay[me]["send_displs"][d + 1] - lay[me]["send_displs"][d]
+            assert sent == lay[d]["recv_counts"][me]
+    assert sum(int(l["recv_displs"][-1]) for l in lay) == int(m.sum())
+
+
 ALL_PINS = [
     pin_sigmoid_exact, pin_sigmoid_symmetry, pin_bf16_rounding, pin_selection_brute_force,
     pin_selection_exhaustive, pin_selection_kimi_shape, pin_plain_topk, pin_keep_all_groups_is_noop,
     pin_weights, pin_histogram_scan_perm, pin_invariants, pin_rank_local_matrix, pin_page_facts,
     pin_router_gemm, pin_rejects_invalid, pin_layout_inverse, pin_layout_tile_one, pin_layout_append,
-    pin_layout_invariants, pin_layout_rejects,
+    pin_layout_invariants, pin_layout_rejects, pin_route_index, pin_token_sharded,
+    pin_dispatch_counts, pin_alltoall_layout,
 ]

@@ -55,6 +55,11 @@ MUTANTS = {
                         "        if (padded_rows) padded_rows[r] = 0;"),
     "layout_bin_index_shifted": ("            if (m_indices) m_indices[poff[e] + i] = e;",
                                  "            if (m_indices) m_indices[poff[e] + i] = e + 1;"),
+    "index_weight_bits_as_id": ("        int l = (int)((uint32_t)packed[i] >> 16);\n        perm[cursor[l]] = (int32_t)i;",
+                                "        int l = (int)((uint32_t)packed[i] >> 16);\n        perm[cursor[l]] = (int32_t)(n - 1 - i);"),
+    "dispatch_interleaved_ranks": ("        send_counts[ids[i] / per] += 1;", "        send_counts[ids[i] % R] += 1;"),
+    "alltoall_row_for_column": ("        recv_counts[s] = matrix[(size_t)s * R + me];",
+                                "        recv_counts[s] = matrix[(size_t)me * R + s];"),
 }
 
 # cheap pins first; the exhaustive sigmoid sweep last
