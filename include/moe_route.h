@@ -59,7 +59,8 @@ typedef enum {
     MOE_ROUTE_E_UNSUPPORTED = -2,    /* valid, but not a shape the kernels implement */
     MOE_ROUTE_E_CUDA = -3,           /* a CUDA runtime call failed (launch, allocation) */
     MOE_ROUTE_E_WORKSPACE = -4,      /* per-device state missing while the stream is capturing */
-    MOE_ROUTE_E_DEVICE_TIMEOUT = -5  /* a bounded device-side wait ran out (see device_status) */
+    MOE_ROUTE_E_DEVICE_TIMEOUT = -5, /* a bounded device-side wait ran out (see device_status) */
+    MOE_ROUTE_E_BAD_ID = -6          /* moe_route_index: an id >= NE or repeated in a row (device_status) */
 } moe_route_status;
 
 typedef enum { MOE_ROUTE_F32 = 0, MOE_ROUTE_BF16 = 1 } moe_route_dtype;
@@ -137,6 +138,50 @@ int moe_route_layout(const int32_t* counts, const int32_t* offsets, const int32_
                      int32_t* padded_rows, int32_t* m_indices, int capacity,
                      struct CUstream_st* stream);
 
+/*
+ * moe_route_index -- steps a9..a11 alone: counts, offsets and the stable (id, token, slot)
+ * permutation of given packed values (id << 16 | weight).  For token-sharded routing:
+ * each rank routes a contiguous slice of the tokens and the top-k results are gathered
+ * (vLLM PR #59693, description of the token-sharded path); routing is row-independent,
+ * so the gathered packed values are those of the whole batch, and this call gives every
+ * rank the whole batch's counts, offsets and perm without routing the other slices.
+ *   packed  [T, k] int32, device; ids must be < NE and distinct within each row (as every
+ *           routing writes them; the ranks count the rows that hold an id).
+ *   counts [NE], offsets [NE + 1], perm [T * k]: device outputs, as moe_route defines them.
+ * Errors: INVALID_ARG for T < 0, k < 1, NE < 1, NULL pointers, T * k >= 2^31;
+ * UNSUPPORTED for k > 32 or NE > 1,056.  An id >= NE, or an id repeated within a row, is
+ * left out of every output and moe_route_device_status() then returns
+ * MOE_ROUTE_E_BAD_ID (outputs unspecified, every write stays inside the arrays).
+ */
+int moe_route_index(const int32_t* packed, int T, int k, int NE, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, struct CUstream_st* stream);
+
+/*
+ * moe_route_dispatch_counts -- expert-parallel dispatch: num_ranks ranks own contiguous
+ * ranges of E / num_ranks experts; from the offsets of a routing with GLOBAL ids
+ * (local_count = 0, NE = E), send_offsets[d] = offsets[d * E / num_ranks] (num_ranks + 1)
+ * and send_counts[d] = send_offsets[d + 1] - send_offsets[d].  The entries for rank d are
+ * perm[send_offsets[d] .. send_offsets[d + 1]), already in (expert, token, slot) order.
+ * The counts are one row of the counts matrix of a variable-size all-to-all (vLLM PR
+ * #54606, description of its collectives).  Errors: INVALID_ARG for E % num_ranks != 0,
+ * num_ranks < 1, NULL offsets.  Device pointers; one small kernel.
+ */
+int moe_route_dispatch_counts(const int32_t* offsets, int E, int num_ranks, int32_t* send_counts,
+                              int32_t* send_offsets, struct CUstream_st* stream);
+
+/*
+ * moe_route_alltoall_layout -- rank `rank`'s view of the gathered counts matrix
+ * matrix[num_ranks][num_ranks] (row = source rank, column = destination rank; device):
+ *   send_displs [num_ranks + 1] = exclusive scan of row `rank`
+ *   recv_counts [num_ranks]     = column `rank`
+ *   recv_displs [num_ranks + 1] = exclusive scan of that column
+ * Outputs nullable.  Errors: INVALID_ARG for rank outside [0, num_ranks), NULL matrix;
+ * UNSUPPORTED for num_ranks > 1,024.  One small kernel.
+ */
+int moe_route_alltoall_layout(const int32_t* matrix, int num_ranks, int rank, int32_t* send_displs,
+                              int32_t* recv_counts, int32_t* recv_displs,
+                              struct CUstream_st* stream);
+
 /* Rows the padded layout can need for any routing of T rows: T * k + NE * (tile - 1);
  * MOE_ROUTE_E_INVALID_ARG for invalid arguments or a bound beyond 2^31 - 1. */
 int moe_route_padded_capacity(int T, int k, int NE, int tile);
@@ -161,8 +206,8 @@ int moe_route_reserve(void);
 
 /*
  * Waits for the current device, returns and clears the device-side error word
- * (MOE_ROUTE_OK or MOE_ROUTE_E_DEVICE_TIMEOUT), and resets the workspace's barrier
- * state after an error.
+ * (MOE_ROUTE_OK, MOE_ROUTE_E_DEVICE_TIMEOUT or MOE_ROUTE_E_BAD_ID), and resets the
+ * workspace's barrier state after an error.
  */
 int moe_route_device_status(void);
 

@@ -22,6 +22,7 @@ E_UNSUPPORTED = -2
 E_CUDA = -3
 E_WORKSPACE = -4
 E_DEVICE_TIMEOUT = -5
+E_BAD_ID = -6
 F32 = 0
 BF16 = 1
 
@@ -67,6 +68,12 @@ def load(path: str | None = None):
     lib.moe_route_layout.restype = I
     lib.moe_route_padded_capacity.argtypes = [I, I, I, I]
     lib.moe_route_padded_capacity.restype = I
+    lib.moe_route_index.argtypes = [P, I, I, I, P, P, P, P]
+    lib.moe_route_index.restype = I
+    lib.moe_route_dispatch_counts.argtypes = [P, I, I, P, P, P]
+    lib.moe_route_dispatch_counts.restype = I
+    lib.moe_route_alltoall_layout.argtypes = [P, I, I, P, P, P, P]
+    lib.moe_route_alltoall_layout.restype = I
     lib.moe_route_empty.argtypes = [I, P]
     lib.moe_route_empty.restype = I
     lib.moe_route_strerror.argtypes = [I]
@@ -224,6 +231,45 @@ def route_layout(out: dict, tile: int = 128, *, k: int | None = None, inv: bool 
                                  capacity, _stream(stream))
     _check(rc, "moe_route_layout")
     return layout
+
+
+def route_index(packed: torch.Tensor, NE: int, *, out: dict | None = None, stream=None) -> dict:
+    """moe_route_index: counts, offsets and perm of packed values [T, k] (int32, CUDA)."""
+    T, k = packed.shape
+    if out is None:
+        out = dict(counts=torch.empty(NE, dtype=torch.int32, device=packed.device),
+                   offsets=torch.empty(NE + 1, dtype=torch.int32, device=packed.device),
+                   perm=torch.empty(T * k, dtype=torch.int32, device=packed.device))
+    rc = load().moe_route_index(_ptr(packed), T, k, NE, _ptr(out["counts"]), _ptr(out["offsets"]),
+                                _ptr(out["perm"]), _stream(stream))
+    _check(rc, "moe_route_index")
+    return out
+
+
+def dispatch_counts(offsets: torch.Tensor, num_ranks: int, stream=None) -> dict:
+    """moe_route_dispatch_counts on the offsets of a global-id routing."""
+    E = offsets.numel() - 1
+    dev = offsets.device
+    out = dict(send_counts=torch.empty(num_ranks, dtype=torch.int32, device=dev),
+               send_offsets=torch.empty(num_ranks + 1, dtype=torch.int32, device=dev))
+    rc = load().moe_route_dispatch_counts(_ptr(offsets), E, num_ranks, _ptr(out["send_counts"]),
+                                          _ptr(out["send_offsets"]), _stream(stream))
+    _check(rc, "moe_route_dispatch_counts")
+    return out
+
+
+def alltoall_layout(matrix: torch.Tensor, rank: int, stream=None) -> dict:
+    """moe_route_alltoall_layout: rank's send/receive layout from the counts matrix."""
+    R = matrix.shape[0]
+    dev = matrix.device
+    out = dict(send_displs=torch.empty(R + 1, dtype=torch.int32, device=dev),
+               recv_counts=torch.empty(R, dtype=torch.int32, device=dev),
+               recv_displs=torch.empty(R + 1, dtype=torch.int32, device=dev))
+    rc = load().moe_route_alltoall_layout(_ptr(matrix.contiguous()), R, rank, _ptr(out["send_displs"]),
+                                          _ptr(out["recv_counts"]), _ptr(out["recv_displs"]),
+                                          _stream(stream))
+    _check(rc, "moe_route_alltoall_layout")
+    return out
 
 
 def empty_kernel(ctas: int = 1, stream=None):

@@ -224,6 +224,58 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
   return launch_route_decode(a, DT_SCORE, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }
 
+int moe_route_index(const int32_t* packed, int T, int k, int NE, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, struct CUstream_st* stream) {
+  if (T < 0 || k < 1 || NE < 1) return MOE_ROUTE_E_INVALID_ARG;
+  if (static_cast<long long>(T) * k >= (1ll << 31)) return MOE_ROUTE_E_INVALID_ARG;
+  if (!counts || !offsets || (T > 0 && (!packed || !perm))) return MOE_ROUTE_E_INVALID_ARG;
+  if (k > kMaxK || NE > kMaxBins) return MOE_ROUTE_E_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevState* d = nullptr;
+  const int rc = get_state(st, &d);
+  if (rc != MOE_ROUTE_OK) return rc;
+  RouteArgs a = {};
+  a.logits = packed;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.err = d->err;
+  a.T = T;
+  a.k = k;
+  a.Kg = 0;
+  a.NE = NE;
+  cudaError_t ce;
+  if (T <= 64) {
+    ce = launch_route_decode(a, DT_PACKED, st);
+  } else {
+    int grid = (T + 15) / 16;
+    if (grid > d->pw.grid_max) grid = d->pw.grid_max;
+    ce = launch_route_prefill(a, DT_PACKED, d->pw, grid, st);
+  }
+  return ce == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
+}
+
+int moe_route_dispatch_counts(const int32_t* offsets, int E, int num_ranks, int32_t* send_counts,
+                              int32_t* send_offsets, struct CUstream_st* stream) {
+  if (!offsets || E < 1 || num_ranks < 1 || E % num_ranks != 0) return MOE_ROUTE_E_INVALID_ARG;
+  if (!send_counts && !send_offsets) return MOE_ROUTE_OK;
+  return launch_dispatch_counts(offsets, E, num_ranks, send_counts, send_offsets,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_ROUTE_OK
+             : MOE_ROUTE_E_CUDA;
+}
+
+int moe_route_alltoall_layout(const int32_t* matrix, int num_ranks, int rank, int32_t* send_displs,
+                              int32_t* recv_counts, int32_t* recv_displs,
+                              struct CUstream_st* stream) {
+  if (!matrix || num_ranks < 1 || rank < 0 || rank >= num_ranks) return MOE_ROUTE_E_INVALID_ARG;
+  if (num_ranks > 1024) return MOE_ROUTE_E_UNSUPPORTED;
+  return launch_alltoall_layout(matrix, num_ranks, rank, send_displs, recv_counts, recv_displs,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_ROUTE_OK
+             : MOE_ROUTE_E_CUDA;
+}
+
 int moe_route_padded_capacity(int T, int k, int NE, int tile) {
   if (T < 0 || k < 1 || NE < 1 || tile < 1) return MOE_ROUTE_E_INVALID_ARG;
   const long long cap = static_cast<long long>(T) * k + static_cast<long long>(NE) * (tile - 1);
@@ -312,6 +364,7 @@ const char* moe_route_strerror(int status) {
     case MOE_ROUTE_E_CUDA: return "CUDA runtime error";
     case MOE_ROUTE_E_WORKSPACE: return "library state missing during stream capture";
     case MOE_ROUTE_E_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case MOE_ROUTE_E_BAD_ID: return "a packed id is not below the number of bins or repeats in a row";
     default: return "unknown status";
   }
 }

@@ -31,6 +31,10 @@ struct LayoutArgs {
 };
 
 cudaError_t launch_route_layout(const LayoutArgs& g, int nsm, cudaStream_t st);
+cudaError_t launch_dispatch_counts(const int32_t* offsets, int E, int R, int32_t* send_counts,
+                                   int32_t* send_offsets, cudaStream_t st);
+cudaError_t launch_alltoall_layout(const int32_t* matrix, int R, int me, int32_t* send_displs,
+                                   int32_t* recv_counts, int32_t* recv_displs, cudaStream_t st);
 cudaError_t launch_sigmoid_table(float* tab, float2* etab, cudaStream_t st);
 cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const float2* etab, float* s,
                            int n, cudaStream_t st);

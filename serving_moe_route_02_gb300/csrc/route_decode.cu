@@ -30,11 +30,12 @@ __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / 
 
 template <int DT>
 struct DecodeSmem {
-  static constexpr int ROWB = (DT == DT_BF16) ? kE * 2 : kE * 4;
+  static constexpr int ROWB = (DT == DT_PACKED) ? 0 : (DT == DT_BF16) ? kE * 2 : kE * 4;
   static constexpr int STAB = (DT == DT_BF16) ? kSigTablePad * 4 : 0;
+  static constexpr int BIASB = (DT == DT_PACKED) ? 0 : kE * 4;
   static constexpr int o_stab = 0;
   static constexpr int o_bias = align_up(o_stab + STAB, 128);  // (scores: no table)
-  static constexpr int o_rows = align_up(o_bias + kE * 4, 128);
+  static constexpr int o_rows = align_up(o_bias + BIASB, 128);
   static constexpr int o_ws = align_up(o_rows + kDecodeRowsPerCta * ROWB, 128);
   static constexpr int o_lid = align_up(o_ws + kDecodeRowsPerCta * int(sizeof(WarpScratch)), 128);
   static constexpr int o_offs = align_up(o_lid + 64 * kMaxK * 4, 128);  // lid: [64 rows][32]
@@ -47,6 +48,7 @@ struct DecodeSmem {
 static_assert(DecodeSmem<DT_F32>::total <= 227 * 1024, "decode smem (f32) exceeds 227 KB");
 static_assert(DecodeSmem<DT_BF16>::total <= 227 * 1024, "decode smem (bf16) exceeds 227 KB");
 static_assert(DecodeSmem<DT_SCORE>::total <= 227 * 1024, "decode smem (scores) exceeds 227 KB");
+static_assert(DecodeSmem<DT_PACKED>::total <= 227 * 1024, "decode smem (index) exceeds 227 KB");
 static_assert(kDecodeRowsPerCta * kDecodeMaxCtas <= 64, "row masks are 64 bits");
 
 // Exclusive scan over the bins of counts popc(mask[e]) into offs[0..n], offs[n] = total;
@@ -99,8 +101,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   const int nctas = static_cast<int>(cluster.num_blocks());
   const int row0 = crank * kDecodeRowsPerCta;
   const int nrows = max(0, min(kDecodeRowsPerCta, a.T - row0));
-  const uint32_t bytes = uint32_t(nrows) * L::ROWB + uint32_t(L::STAB) + uint32_t(kE * 4);
-  const bool have = nrows > 0;  // CTAs without rows (T = 0) load nothing
+  const uint32_t bytes = uint32_t(nrows) * L::ROWB + uint32_t(L::STAB) + uint32_t(L::BIASB);
+  const bool have = DT != DT_PACKED && nrows > 0;  // CTAs without rows (T = 0) load nothing
 
   if (tid == 0) {
     mbar_init(mbar, 1);
@@ -129,7 +131,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   if (have) mbar_wait_bounded(mbar, 0, a.err);
 
   SlotOut o = {};
-  if (w < nrows) {
+  if constexpr (DT == DT_PACKED) {
+    // index mode: the row's ids come from the given packed values; an id at or above
+    // the bin count is reported and left out (-1)
+    if (w < nrows && lane < a.k) {
+      const int t = row0 + w;
+      o.lid = int(uint32_t(static_cast<const int32_t*>(a.logits)[size_t(t) * a.k + lane]) >> 16);
+      // ids must be distinct within a row (the ranks below count rows per id)
+      const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
+      const bool repeated = __popc(__match_any_sync(kmask, o.lid)) > 1;
+      if (o.lid >= a.NE || repeated) {
+        atomicExch(a.err, kErrBadId);
+        o.lid = -1;
+      }
+      lid_all[t * kMaxK + lane] = o.lid;
+    }
+  } else if (w < nrows) {
     o = route_row<DT, SPEC ? 16 : 0, SPEC ? 4 : 0>(rows + w * L::ROWB, bias_s, stab, a, wsp[w]);
     const int t = row0 + w;
     if (lane < a.k) {
@@ -163,7 +180,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   uint32_t* mask32 = reinterpret_cast<uint32_t*>(mask_s);
   for (int x = tid; x < a.T * a.k; x += kDecodeThreads) {
     const int t = x / a.k, j = x - t * a.k;
-    atomicOr(mask32 + 2 * lid_all[t * kMaxK + j] + (t >> 5), 1u << (t & 31));
+    const int l = lid_all[t * kMaxK + j];
+    if (DT != DT_PACKED || l >= 0) atomicOr(mask32 + 2 * l + (t >> 5), 1u << (t & 31));
   }
   __syncthreads();
 
@@ -175,7 +193,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     }
     if (tid == 0) a.offsets[a.NE] = offs_s[a.NE];
   }
-  if (w < nrows && lane < a.k) {
+  if (w < nrows && lane < a.k && (DT != DT_PACKED || o.lid >= 0)) {
     const int t = row0 + w;
     const int pos = offs_s[o.lid] + __popcll(mask_s[o.lid] & ((1ull << t) - 1ull));
     a.perm[pos] = t * a.k + lane;
@@ -254,6 +272,7 @@ cudaError_t setup_decode_kernels() {
   if ((e = set_decode_smem<DT_BF16, false>()) != cudaSuccess) return e;
   if ((e = set_decode_smem<DT_BF16, true>()) != cudaSuccess) return e;
   if ((e = set_decode_smem<DT_SCORE, false>()) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_PACKED, false>()) != cudaSuccess) return e;
   return set_decode_smem<DT_SCORE, true>();
 }
 
@@ -282,6 +301,7 @@ cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) 
   const bool spec = a.k == 16 && a.Kg == 4;
   if (dtype == DT_BF16) return spec ? launch_decode_t<DT_BF16, true>(cfg, a) : launch_decode_t<DT_BF16, false>(cfg, a);
   if (dtype == DT_SCORE) return spec ? launch_decode_t<DT_SCORE, true>(cfg, a) : launch_decode_t<DT_SCORE, false>(cfg, a);
+  if (dtype == DT_PACKED) return launch_decode_t<DT_PACKED, false>(cfg, a);
   return spec ? launch_decode_t<DT_F32, true>(cfg, a) : launch_decode_t<DT_F32, false>(cfg, a);
 }
 

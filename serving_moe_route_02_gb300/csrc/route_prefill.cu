@@ -31,9 +31,11 @@ __host__ __device__ constexpr int p_align(int x, int a) { return (x + a - 1) / a
 template <int DT, bool SPEC>
 struct PrefillSmem {
   static constexpr bool WIDE = (DT == DT_BF16) && SPEC;
+  static constexpr bool INDEX = DT == DT_PACKED;              // histogram/scan/perm of packed ids
   static constexpr int NW = WIDE ? 24 : 16;                  // warps per CTA
-  static constexpr int ROWB = (DT == DT_BF16) ? kE * 2 : kE * 4;
-  static constexpr int D = WIDE ? 2 : ((DT == DT_BF16) ? 3 : 2);  // rows in flight per warp
+  // (index mode streams no rows: its "ring" is only phase-3 room)
+  static constexpr int ROWB = INDEX ? 4096 : (DT == DT_BF16) ? kE * 2 : kE * 4;
+  static constexpr int D = INDEX ? 1 : WIDE ? 2 : ((DT == DT_BF16) ? 3 : 2);  // rows in flight
   static constexpr int NB = SPEC ? 4 * kLanesPerGroup * kEPL : kEPL * 32;
   using WS = WarpScratchT<NB>;
   static constexpr int STAB = (DT == DT_BF16) ? kSigTablePad * 4 : 0;
@@ -55,6 +57,8 @@ static_assert(PrefillSmem<DT_F32, false>::total <= 227 * 1024, "prefill smem (f3
 static_assert(PrefillSmem<DT_F32, true>::total <= 227 * 1024, "prefill smem (f32) exceeds 227 KB");
 static_assert(PrefillSmem<DT_BF16, false>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
 static_assert(PrefillSmem<DT_BF16, true>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
+static_assert(PrefillSmem<DT_PACKED, false>::total <= 227 * 1024, "prefill smem (index) exceeds 227 KB");
+static_assert(PrefillSmem<DT_PACKED, false>::STAGE_INTS >= 4 * kMaxK, "index mode phase-3 room");
 static_assert(PrefillSmem<DT_BF16, true>::STAGE_INTS >= 4 * kMaxK &&
                   PrefillSmem<DT_BF16, false>::STAGE_INTS >= 4 * kMaxK &&
                   PrefillSmem<DT_F32, true>::STAGE_INTS >= 4 * kMaxK &&
@@ -167,6 +171,9 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   uint64_t* mb = mbar_all + w * L::D;
   const uint8_t* logits = static_cast<const uint8_t*>(a.logits);
 
+  // packed ids phase 3 reads: written by phase 1, or given (index mode)
+  const int32_t* pk = L::INDEX ? static_cast<const int32_t*>(a.logits) : a.packed;
+
   // ---- setup: mbarriers, histogram, score table and bias, first rows in flight
   if (lane == 0) {
     for (int d = 0; d < L::D; ++d) mbar_init(mb + d, 1);
@@ -179,6 +186,29 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   }
   for (int e = tid; e < a.NE; e += NT) hist_s[e] = 0;
   __syncthreads();
+  if constexpr (L::INDEX) {
+    // ---- phase 1 (index mode): count this warp's given packed ids, 8 rows of loads in
+    //      flight; an id at or above the bin count is reported and left out
+    for (int i0 = 0; i0 < nw; i0 += 8) {
+      int32_t v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = (i0 + q < nw && lane < a.k) ? pk[size_t(wr0 + i0 + q) * a.k + lane] : 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (i0 + q < nw) {
+          // ids must be distinct within a row: a repeated id is reported and left out
+          // here and in phase 3 alike
+          const int l = (lane < a.k) ? int(uint32_t(v[q]) >> 16) : -1 - lane;
+          const bool repeated = __popc(__match_any_sync(0xffffffffu, l)) > 1;
+          if (lane < a.k) {
+            if (l < a.NE && !repeated) atomicAdd(&hist_s[l], 1);
+            else atomicExch(a.err, kErrBadId);
+          }
+        }
+      }
+    }
+  } else {
   if (tid == 0) {
     mbar_expect_tx(tab_bar, uint32_t(L::STAB + kE * 4));
     if (L::STAB) bulk_g2s(stab, a.stab, L::STAB, tab_bar);
@@ -211,6 +241,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
       mbar_expect_tx(mb + slot, L::ROWB);
       bulk_g2s(ring + slot * L::ROWB, logits + size_t(t + L::D) * L::ROWB, L::ROWB, mb + slot);
     }
+  }
   }
   __syncthreads();
   for (int e = tid; e < a.NE; e += NT) pw.hist[size_t(e) * pw.grid_max + cta] = hist_s[e];
@@ -278,7 +309,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
   auto stage_chunk = [&](int c0) {
     const int n = min(chunk_rows, nw - c0) * a.k;
-    const int32_t* src = a.packed + size_t(wr0 + c0) * a.k;
+    const int32_t* src = pk + size_t(wr0 + c0) * a.k;
     for (int i0 = 0; i0 < n; i0 += 8 * 32) {
       int32_t v[8];
 #pragma unroll
@@ -302,7 +333,16 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
     stage_chunk(c0);
     const int nr = min(chunk_rows, nw - c0);
     if (lane < a.k)
-      for (int r = 0; r < nr; ++r) atomicAdd(&wpre[int(uint32_t(stage[r * a.k + lane]) >> 16)], 1);
+      for (int r = 0; r < nr; ++r) {
+        const int l = int(uint32_t(stage[r * a.k + lane]) >> 16);
+        bool use = true;
+        if constexpr (L::INDEX) {
+          // every lane of kmask takes part in the match, whatever its id
+          const unsigned same = __match_any_sync(kmask, l);
+          use = l < a.NE && __popc(same) == 1;
+        }
+        if (use) atomicAdd(&wpre[l], 1);
+      }
     __syncwarp();
   }
   __syncthreads();
@@ -324,9 +364,17 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
     if (lane < a.k) {
       for (int r = 0; r < nr; ++r) {
         const int l = int(uint32_t(stage[r * a.k + lane]) >> 16);
-        const int rk = wpre[l];
-        wpre[l] = rk + 1;
-        a.perm[base_s[l] + rk] = (wr0 + c0 + r) * a.k + lane;
+        bool use = true;
+        if constexpr (L::INDEX) {
+          // every lane of kmask takes part in the match, whatever its id
+          const unsigned same = __match_any_sync(kmask, l);
+          use = l < a.NE && __popc(same) == 1;
+        }
+        if (use) {
+          const int rk = wpre[l];
+          wpre[l] = rk + 1;
+          a.perm[base_s[l] + rk] = (wr0 + c0 + r) * a.k + lane;
+        }
         __syncwarp(kmask);  // the next row may count the same bin in another lane
       }
     }
@@ -356,6 +404,7 @@ cudaError_t setup_prefill_kernels(int* blocks_per_sm) {
   if ((e = set_prefill_smem<DT_F32, true>(&b)) != cudaSuccess) return e;
   if ((e = set_prefill_smem<DT_BF16, false>(&b)) != cudaSuccess) return e;
   if ((e = set_prefill_smem<DT_BF16, true>(&b)) != cudaSuccess) return e;
+  if ((e = set_prefill_smem<DT_PACKED, false>(&b)) != cudaSuccess) return e;
   *blocks_per_sm = b;
   return cudaSuccess;
 }
@@ -381,6 +430,7 @@ cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS&
                                  cudaStream_t st) {
   if (!prefill_fits(a.T, grid)) return cudaErrorInvalidValue;
   const bool spec = a.k == 16 && a.Kg == 4;
+  if (dtype == DT_PACKED) return launch_t<DT_PACKED, false>(a, ws, grid, st);
   if (dtype == DT_BF16)
     return spec ? launch_t<DT_BF16, true>(a, ws, grid, st) : launch_t<DT_BF16, false>(a, ws, grid, st);
   return spec ? launch_t<DT_F32, true>(a, ws, grid, st) : launch_t<DT_F32, false>(a, ws, grid, st);

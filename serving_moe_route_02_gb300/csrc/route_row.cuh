@@ -49,9 +49,10 @@ struct WarpScratchT {
 };
 using WarpScratch = WarpScratchT<kEPL * 32>;
 
-// Row input kinds: float32 logits, bfloat16 logits, or float32 scores already equal to
-// sigmoid(logit) (the fused contraction computes them in its epilogue).
-enum { DT_F32 = 0, DT_BF16 = 1, DT_SCORE = 2 };
+// Row input kinds: float32 logits, bfloat16 logits, float32 scores already equal to
+// sigmoid(logit) (the fused contraction computes them in its epilogue), or packed
+// values (id << 16 | weight) that are only indexed (histogram, scan, permutation).
+enum { DT_F32 = 0, DT_BF16 = 1, DT_SCORE = 2, DT_PACKED = 3 };
 
 template <int DT>
 __device__ __forceinline__ float row_sigmoid(const void* row, int e, const float* stab,
