@@ -13,8 +13,9 @@ bit of a normal draw may differ between CPU architectures; nothing stores a
 generated input, every comparison regenerates both sides from the seed.
 
 Workload shapes follow the Kimi-K3 routing described on the pages: 896 routed
-experts, top_k 16, 8 groups of 112 (sglang PR #37, description: "Tier<896, 16>",
-"112 of 896 at EP8"); hidden 7168 for the router contraction.
+experts, top_k 16, 8 groups of 112 (sglang PR #37, description: FlashInfer's
+Tier<896, 16> specialisation, 112 experts per rank at EP8); hidden 7168 for the router
+contraction.
 """
 from __future__ import annotations
 

@@ -3,8 +3,8 @@
  *
  * One routing call, per token row t of a [T, E] logit matrix:
  *   s_e = sigmoid(logit_e); b_e = s_e + bias_e            (a1, a2)
- *     "a sigmoid router with correction bias and grouped top-k"
- *     -- vLLM PR #59693 (ROCm token-sharded residual), description of its KimiMoE test.
+ *     -- vLLM PR #59693 (ROCm token-sharded residual), description of its KimiMoE
+ *        test: the router is a sigmoid with a correction bias and group-limited top-k.
  *   group score = sum of the two largest b of each group of E/n_group consecutive
  *   experts; keep the topk_group groups with the largest score (ties: lower group);
  *   choose the k largest b among the kept experts (ties: lower expert id); slot j
@@ -14,18 +14,21 @@
  *   local_count) become 0..local_count-1, any other expert in slot j becomes
  *   local_count + j; num_experts NE = round_up(local_count + k, 4)         (a7)
  *   packed[t][j] = (id << 16) | bits(w_j)                                  (a8)
- *     -- sglang PR #37 "Rank-local expert ids for the EP routed MoE", description
- *        ("packed (id << 16 | bf16 weight) ids"; "the rank's experts as 0..count-1
- *        and any other expert in top-k slot k as count + k (unique per row)";
- *        "num_experts = round_up(count + top_k, 4)").
+ *     -- sglang PR #37 (rank-local expert ids for the EP routed MoE), description:
+ *        the fused route epilogue packs each slot as the expert id above the bf16
+ *        weight bits; with a staged expert range the rank's own experts become
+ *        0..count-1, every other expert takes count plus its slot index (so ids stay
+ *        unique in a row), and the runner passes count + top_k rounded up to a
+ *        multiple of 4 as the number of experts.
  * and over all rows:
  *   counts[e]  = number of entries with (relabelled) id e, e in [0, NE)     (a9)
  *   offsets    = exclusive scan of counts, offsets[NE] = T * k              (a10)
  *   perm[offsets[e] + r] = t * k + j for the r-th entry of id e in (t, j) order (a11)
- *     -- same passage: "the same (token, local expert, weight) entries reach the
- *        expert GEMMs in the same order".
+ *     -- same passage: whichever ids are used, the expert GEMMs receive the same
+ *        (token, local expert, weight) entries in the same order.
  * The Kimi-K3 instance is E = 896, k = 16, n_group = 8 (112 experts each),
- * topk_group = 4, scale = 2.5 (sglang PR #37: "Tier<896, 16>", "112 of 896 at EP8").
+ * topk_group = 4, scale = 2.5 (sglang PR #37: FlashInfer's Tier<896, 16> routing
+ * specialisation; each of 8 expert-parallel ranks owns 112 of the 896 experts).
  *
  * Conventions for every entry point:
  *   - All array pointers are DEVICE pointers owned by the caller; the library never
@@ -92,7 +95,8 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
  * moe_router_gemm_route -- router contraction a0 fused in front of moe_route:
  *   logits[t][e] = sum_h hidden[t][h] * w_router[e][h], bf16 inputs, fp32 accumulate,
  * then steps a1..a11 on those fp32 logits.  The router weight is 896 x 7168 per layer
- * (HartsyInference PR #798, "Memory per GPU": router 0.59 B parameters over 92 layers).
+ * (HartsyInference PR #798, section Memory per GPU: 0.59 B router parameters over 92
+ * layers).
  *   hidden      [T, H] bf16 bits, 16-byte aligned; w_router [E, H] bf16 bits (row e =
  *               expert e), 16-byte aligned.  H % 64 == 0.
  *   1 <= T <= 64 (decode batches).

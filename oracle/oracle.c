@@ -9,12 +9,12 @@
  * Citations:
  *   sigmoid router, correction bias, grouped top-k:
  *       vLLM PR #59693 (ROCm token-sharded residual), description of the test
- *       KimiMoE ("a sigmoid router with correction bias and grouped top-k").
+ *       KimiMoE (sigmoid scores, a correction bias, group-limited top-k).
  *   packed (id << 16 | bf16 weight), rank-local relabel, round_up(count+top_k, 4),
  *   same entries in the same order for the expert GEMMs:
- *       sglang PR #37 "Rank-local expert ids for the EP routed MoE", description.
+ *       sglang PR #37 (rank-local expert ids for the EP routed MoE), description.
  *   router parameter count (896 x 7168 per layer):
- *       HartsyInference PR #798, "Memory per GPU" (router 0.59 B replicated).
+ *       HartsyInference PR #798, section Memory per GPU (0.59 B router parameters).
  *
  * Built with -O2 -ffp-contract=off and without fast-math so that every float
  * operation is one IEEE operation in the order written.

@@ -6,12 +6,12 @@
  * the CUDA path and the CUDA path never calls it.
  *
  * What it computes (per token row t, then over all rows):
- *   s_e  = sigmoid(logit_e)            "a sigmoid router" (vLLM PR #59693, description)
- *   b_e  = s_e + bias_e                "with correction bias"  (same passage)
- *   group-limited top-k over b          "and grouped top-k"    (same passage)
+ *   s_e  = sigmoid(logit_e)             sigmoid router (vLLM PR #59693, description)
+ *   b_e  = s_e + bias_e                 correction bias (same passage)
+ *   group-limited top-k over b          grouped top-k (same passage)
  *   weights = s of the chosen experts renormalised to `scale`, rounded to bf16
  *   packed  = (id << 16) | bf16 weight bits
- *                         (sglang PR #37, description: "packed (id << 16 | bf16 weight) ids")
+ *                         (sglang PR #37, description: the packed format of the fused route)
  *   optional rank-local relabel (same passage: the rank's experts become
  *   0..count-1, any other expert in top-k slot k becomes count + k,
  *   num_experts = round_up(count + top_k, 4))
