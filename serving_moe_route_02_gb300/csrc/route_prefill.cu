@@ -48,9 +48,16 @@ struct PrefillSmem {
   static constexpr int o_tmp = p_align(o_base + (kMaxBins + 1) * 4, 128);
   static constexpr int o_mbar = p_align(o_tmp + 33 * 4, 128);
   static constexpr int total = o_mbar + NW * D * 8 + 64;
-  // phase 3 reuses [o_ring, o_hist): warp prefixes, then a staging buffer per warp
-  static constexpr int REGION = o_hist - o_ring;
-  static constexpr int STAGE_INTS = (REGION / 4 - NW * kMaxBins) / NW;
+  // phase 3 reuses [0, o_hist) (score table, bias, ring, scratch): warp prefixes, a
+  // staging buffer per warp, the CTA-local bin offsets, then the CTA's entries sorted by
+  // bin (values, then bins) when they fit
+  static constexpr int STAGE_INTS = 256;
+  static constexpr int o3_wpre = 0;
+  static constexpr int o3_stage = o3_wpre + NW * kMaxBins * 4;
+  static constexpr int o3_lbase = o3_stage + NW * STAGE_INTS * 4;
+  static constexpr int o3_sval = p_align(o3_lbase + (kMaxBins + 1) * 4, 16);
+  static constexpr int SORT_CAP = (o_hist - o3_sval) / 6 / 8 * 8;
+  static constexpr int o3_sbin = o3_sval + SORT_CAP * 4;
 };
 
 static_assert(PrefillSmem<DT_F32, false>::total <= 227 * 1024, "prefill smem (f32) exceeds 227 KB");
@@ -58,12 +65,11 @@ static_assert(PrefillSmem<DT_F32, true>::total <= 227 * 1024, "prefill smem (f32
 static_assert(PrefillSmem<DT_BF16, false>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
 static_assert(PrefillSmem<DT_BF16, true>::total <= 227 * 1024, "prefill smem (bf16) exceeds 227 KB");
 static_assert(PrefillSmem<DT_PACKED, false>::total <= 227 * 1024, "prefill smem (index) exceeds 227 KB");
-static_assert(PrefillSmem<DT_PACKED, false>::STAGE_INTS >= 4 * kMaxK, "index mode phase-3 room");
-static_assert(PrefillSmem<DT_BF16, true>::STAGE_INTS >= 4 * kMaxK &&
-                  PrefillSmem<DT_BF16, false>::STAGE_INTS >= 4 * kMaxK &&
-                  PrefillSmem<DT_F32, true>::STAGE_INTS >= 4 * kMaxK &&
-                  PrefillSmem<DT_F32, false>::STAGE_INTS >= 4 * kMaxK,
-              "phase 3 needs room for a few staged rows per warp");
+static_assert(PrefillSmem<DT_PACKED, false>::SORT_CAP >= 4096 && PrefillSmem<DT_BF16, true>::SORT_CAP >= 4096 &&
+                  PrefillSmem<DT_BF16, false>::SORT_CAP >= 4096 &&
+                  PrefillSmem<DT_F32, true>::SORT_CAP >= 4096 &&
+                  PrefillSmem<DT_F32, false>::SORT_CAP >= 4096,
+              "phase 3 keeps room for the CTA-local sort");
 static_assert(PrefillSmem<DT_BF16, true>::ROWB % 128 == 0 && PrefillSmem<DT_F32, true>::ROWB % 128 == 0,
               "row slots keep 128-byte alignment");
 
@@ -76,7 +82,7 @@ __device__ bool grid_barrier(unsigned* bar, unsigned nblocks, int* err, int* fla
   if (threadIdx.x == 0) {
     const unsigned add = (blockIdx.x == 0) ? 0x80000000u - (nblocks - 1u) : 1u;
     unsigned old;
-    __threadfence();
+    // release: the CTA's writes ordered before it by the block barrier above
     asm volatile("atom.release.gpu.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(bar), "r"(add) : "memory");
     int ok = 1;
     const uint64_t t0 = globaltimer_ns();
@@ -90,7 +96,6 @@ __device__ bool grid_barrier(unsigned* bar, unsigned nblocks, int* err, int* fla
         break;
       }
     }
-    __threadfence();
     *flag_s = ok;
   }
   __syncthreads();
@@ -245,6 +250,9 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   }
   __syncthreads();
   for (int e = tid; e < a.NE; e += NT) pw.hist[size_t(e) * pw.grid_max + cta] = hist_s[e];
+  // CTA-local bin offsets of this CTA's entries (the ring and the scratch are free now)
+  int* lbase_s = reinterpret_cast<int*>(smem + L::o3_lbase);
+  block_scan_fast(hist_s, lbase_s, a.NE, tmp);
 
   int* flag_s = tmp + 32;
   if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
@@ -301,9 +309,15 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   // The ring and the routing scratch are free: warp counters [NW][kMaxBins], then a
   // staging buffer per warp for its packed ids, loaded a chunk of rows at a time with
   // all loads of a chunk in flight.
-  int* wpre_all = reinterpret_cast<int*>(ring_all);
+  int* wpre_all = reinterpret_cast<int*>(smem + L::o3_wpre);
   int* wpre = wpre_all + w * kMaxBins;
-  int* stage = wpre_all + NW * kMaxBins + w * L::STAGE_INTS;
+  int* stage = reinterpret_cast<int*>(smem + L::o3_stage) + w * L::STAGE_INTS;
+  int* sval = reinterpret_cast<int*>(smem + L::o3_sval);
+  uint16_t* sbin = reinterpret_cast<uint16_t*>(smem + L::o3_sbin);
+  // the CTA's entries sorted by bin in shared memory, then written as runs (coalesced),
+  // when they fit; otherwise each entry goes straight to its place
+  const int nvalid = lbase_s[a.NE];
+  const bool sorted = nvalid <= L::SORT_CAP;
   const int chunk_rows = L::STAGE_INTS / a.k;
   const int nchunks = (nw + chunk_rows - 1) / chunk_rows;
   const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
@@ -346,9 +360,10 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
     __syncwarp();
   }
   __syncthreads();
-  // warp prefixes per bin
+  // warp prefixes per bin (from the CTA-local bin offset when sorting locally)
   for (int e = tid; e < a.NE; e += NT) {
-    int run = 0;
+    int run = sorted ? lbase_s[e] : 0;
+    if (sorted) base_s[e] -= lbase_s[e];  // global place of local position 0 of bin e
 #pragma unroll 4
     for (int w2 = 0; w2 < NW; ++w2) {
       const int v = wpre_all[w2 * kMaxBins + e];
@@ -373,12 +388,22 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         if (use) {
           const int rk = wpre[l];
           wpre[l] = rk + 1;
-          a.perm[base_s[l] + rk] = (wr0 + c0 + r) * a.k + lane;
+          const int x = (wr0 + c0 + r) * a.k + lane;
+          if (sorted) {
+            sval[rk] = x;
+            sbin[rk] = static_cast<uint16_t>(l);
+          } else {
+            a.perm[base_s[l] + rk] = x;
+          }
         }
         __syncwarp(kmask);  // the next row may count the same bin in another lane
       }
     }
     __syncwarp();
+  }
+  if (sorted) {
+    __syncthreads();
+    for (int i = tid; i < nvalid; i += NT) a.perm[base_s[sbin[i]] + i] = sval[i];
   }
 }
 
