@@ -47,7 +47,10 @@ struct PrefillSmem {
   static constexpr int o_base = p_align(o_hist + (kMaxBins + 1) * 4, 128);
   static constexpr int o_tmp = p_align(o_base + (kMaxBins + 1) * 4, 128);
   static constexpr int o_mbar = p_align(o_tmp + 33 * 4, 128);
-  static constexpr int total = o_mbar + NW * D * 8 + 64;
+  // each warp keeps its rows' relabelled ids (16-bit) for phase 3 in the room left
+  static constexpr int o_lid = p_align(o_mbar + NW * D * 8 + 64, 128);
+  static constexpr int LID_ENTRIES = (227 * 1024 - o_lid) / (NW * 2) / 64 * 64;
+  static constexpr int total = o_lid + NW * LID_ENTRIES * 2;
   // phase 3 reuses [0, o_hist) (score table, bias, ring, scratch): warp prefixes, a
   // staging buffer per warp, the CTA-local bin offsets, then the CTA's entries sorted by
   // bin (values, then bins) when they fit
@@ -55,7 +58,8 @@ struct PrefillSmem {
   static constexpr int o3_wpre = 0;
   static constexpr int o3_stage = o3_wpre + NW * kMaxBins * 4;
   static constexpr int o3_lbase = o3_stage + NW * STAGE_INTS * 4;
-  static constexpr int o3_sval = p_align(o3_lbase + (kMaxBins + 1) * 4, 16);
+  static constexpr int o3_cpre = o3_lbase + (kMaxBins + 1) * 4;
+  static constexpr int o3_sval = p_align(o3_cpre + kMaxBins * 4, 16);
   static constexpr int SORT_CAP = (o_hist - o3_sval) / 6 / 8 * 8;
   static constexpr int o3_sbin = o3_sval + SORT_CAP * 4;
 };
@@ -70,6 +74,10 @@ static_assert(PrefillSmem<DT_PACKED, false>::SORT_CAP >= 4096 && PrefillSmem<DT_
                   PrefillSmem<DT_F32, true>::SORT_CAP >= 4096 &&
                   PrefillSmem<DT_F32, false>::SORT_CAP >= 4096,
               "phase 3 keeps room for the CTA-local sort");
+static_assert(PrefillSmem<DT_BF16, true>::LID_ENTRIES >= 512 && PrefillSmem<DT_BF16, false>::LID_ENTRIES >= 512 &&
+                  PrefillSmem<DT_F32, true>::LID_ENTRIES >= 512 && PrefillSmem<DT_F32, false>::LID_ENTRIES >= 512 &&
+                  PrefillSmem<DT_PACKED, false>::LID_ENTRIES >= 512,
+              "room for the kept ids");
 static_assert(PrefillSmem<DT_BF16, true>::ROWB % 128 == 0 && PrefillSmem<DT_F32, true>::ROWB % 128 == 0,
               "row slots keep 128-byte alignment");
 
@@ -162,6 +170,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   int* base_s = reinterpret_cast<int*>(smem + L::o_base);
   int* tmp = reinterpret_cast<int*>(smem + L::o_tmp);
   uint64_t* mbar_all = reinterpret_cast<uint64_t*>(smem + L::o_mbar);
+  uint16_t* lid16 = reinterpret_cast<uint16_t*>(smem + L::o_lid) + (threadIdx.x >> 5) * L::LID_ENTRIES;
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int grid = gridDim.x, cta = blockIdx.x;
@@ -206,6 +215,8 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
           // here and in phase 3 alike
           const int l = (lane < a.k) ? int(uint32_t(v[q]) >> 16) : -1 - lane;
           const bool repeated = __popc(__match_any_sync(0xffffffffu, l)) > 1;
+          if (lane < a.k && (i0 + q) * a.k + lane < L::LID_ENTRIES)
+            lid16[(i0 + q) * a.k + lane] = static_cast<uint16_t>(l);
           if (lane < a.k) {
             if (l < a.NE && !repeated) atomicAdd(&hist_s[l], 1);
             else atomicExch(a.err, kErrBadId);
@@ -239,6 +250,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
       a.packed[size_t(t) * a.k + lane] = o.packed;
       if (a.ids) a.ids[size_t(t) * a.k + lane] = o.id;
       atomicAdd(&hist_s[o.lid], 1);
+      if (i * a.k + lane < L::LID_ENTRIES) lid16[i * a.k + lane] = static_cast<uint16_t>(o.lid);
     }
     __syncwarp();
     if (lane == 0 && i + L::D < nw) {
@@ -293,8 +305,15 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
 
   if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
 
-  // ---- phase 3: offsets, then this CTA's permutation entries
-  for (int e = tid; e < a.NE; e += NT) hist_s[e] = __ldcg(pw.counts + e);
+  // ---- phase 3: offsets, then this CTA's permutation entries (bin totals and this CTA's
+  //      prefixes are loaded together: one round trip)
+  int* cpre_s = reinterpret_cast<int*>(smem + L::o3_cpre);
+  for (int e = tid; e < a.NE; e += NT) {
+    const int c = __ldcg(pw.counts + e);
+    const int p = __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
+    hist_s[e] = c;
+    cpre_s[e] = p;
+  }
   __syncthreads();
   block_scan_fast(hist_s, base_s, a.NE, tmp);
   if (cta == 0) {
@@ -304,7 +323,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
     }
     if (tid == 0) a.offsets[a.NE] = base_s[a.NE];
   }
-  for (int e = tid; e < a.NE; e += NT) base_s[e] += __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
+  for (int e = tid; e < a.NE; e += NT) base_s[e] += cpre_s[e];
 
   // The ring and the routing scratch are free: warp counters [NW][kMaxBins], then a
   // staging buffer per warp for its packed ids, loaded a chunk of rows at a time with
@@ -318,8 +337,14 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   // when they fit; otherwise each entry goes straight to its place
   const int nvalid = lbase_s[a.NE];
   const bool sorted = nvalid <= L::SORT_CAP;
-  const int chunk_rows = L::STAGE_INTS / a.k;
+  // this warp's ids: kept in shared memory by phase 1 when they fit, otherwise staged
+  // from the packed values a chunk of rows at a time
+  const bool keep = nw * a.k <= L::LID_ENTRIES;
+  const int chunk_rows = keep ? max(nw, 1) : L::STAGE_INTS / a.k;
   const int nchunks = (nw + chunk_rows - 1) / chunk_rows;
+  auto lid_of = [&](int c0, int r) -> int {
+    return keep ? int(lid16[(c0 + r) * a.k + lane]) : int(uint32_t(stage[r * a.k + lane]) >> 16);
+  };
   const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
   auto stage_chunk = [&](int c0) {
     const int n = min(chunk_rows, nw - c0) * a.k;
@@ -344,11 +369,11 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   __syncwarp();
   // this warp's bin counts
   for (int c0 = 0; c0 < nw; c0 += chunk_rows) {
-    stage_chunk(c0);
+    if (!keep) stage_chunk(c0);
     const int nr = min(chunk_rows, nw - c0);
     if (lane < a.k)
       for (int r = 0; r < nr; ++r) {
-        const int l = int(uint32_t(stage[r * a.k + lane]) >> 16);
+        const int l = lid_of(c0, r);
         bool use = true;
         if constexpr (L::INDEX) {
           // every lane of kmask takes part in the match, whatever its id
@@ -373,12 +398,20 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   }
   __syncthreads();
   // the walk: rows in order (the last chunk staged above is still in place)
+  auto place = [&](int l, int rk, int x) {
+    if (sorted) {
+      sval[rk] = x;
+      sbin[rk] = static_cast<uint16_t>(l);
+    } else {
+      a.perm[base_s[l] + rk] = x;
+    }
+  };
   for (int c0 = 0; c0 < nw; c0 += chunk_rows) {
-    if (nchunks > 1) stage_chunk(c0);
+    if (!keep && nchunks > 1) stage_chunk(c0);
     const int nr = min(chunk_rows, nw - c0);
     if (lane < a.k) {
       for (int r = 0; r < nr; ++r) {
-        const int l = int(uint32_t(stage[r * a.k + lane]) >> 16);
+        const int l = lid_of(c0, r);
         bool use = true;
         if constexpr (L::INDEX) {
           // every lane of kmask takes part in the match, whatever its id
@@ -388,13 +421,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         if (use) {
           const int rk = wpre[l];
           wpre[l] = rk + 1;
-          const int x = (wr0 + c0 + r) * a.k + lane;
-          if (sorted) {
-            sval[rk] = x;
-            sbin[rk] = static_cast<uint16_t>(l);
-          } else {
-            a.perm[base_s[l] + rk] = x;
-          }
+          place(l, rk, (wr0 + c0 + r) * a.k + lane);
         }
         __syncwarp(kmask);  // the next row may count the same bin in another lane
       }
