@@ -51,32 +51,29 @@ static_assert(DecodeSmem<DT_SCORE>::total <= 227 * 1024, "decode smem (scores) e
 static_assert(DecodeSmem<DT_PACKED>::total <= 227 * 1024, "decode smem (index) exceeds 227 KB");
 static_assert(kDecodeRowsPerCta * kDecodeMaxCtas <= 64, "row masks are 64 bits");
 
-// Exclusive scan over the bins of counts popc(mask[e]) into offs[0..n], offs[n] = total;
-// two block barriers.  mask[e] holds rows 0..31 in its low word, 32..63 in its high word.
-__device__ __forceinline__ void mask_count_scan(const unsigned long long* mask, int* offs, int n,
-                                                int* tmp) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int lane = tid & 31, wid = tid >> 5;
-  const int per = (n + nt - 1) / nt;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-  int sum = 0;
-  for (int i = lo; i < hi; ++i) sum += __popcll(mask[i]);
-  int incl = sum;
+// Exclusive scan over the bins of counts popc(mask[e]) into offs[0..n], offs[n] = total,
+// by warp 0 alone (lane l takes a contiguous run of bins), then one block barrier.
+// mask[e] holds rows 0..31 in its low word, 32..63 in its high word.
+__device__ __forceinline__ void mask_count_scan(const unsigned long long* mask, int* offs, int n) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int per = (n + 31) / 32;
+    const int lo = min(n, lane * per), hi = min(n, lo + per);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += __popcll(mask[i]);
+    int incl = sum;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      offs[i] = run;
+      run += __popcll(mask[i]);
+    }
+    if (lane == 31) offs[n] = incl;
   }
-  if (lane == 31) tmp[wid] = incl;
-  __syncthreads();
-  int run = incl - sum;
-  for (int i = 0; i < wid; ++i) run += tmp[i];
-  for (int i = lo; i < hi; ++i) {
-    offs[i] = run;
-    run += __popcll(mask[i]);
-  }
-  if (hi == n && lo < hi) offs[n] = run;
-  if (n == 0 && tid == 0) offs[0] = 0;
   __syncthreads();
 }
 
@@ -92,7 +89,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   WarpScratch* wsp = reinterpret_cast<WarpScratch*>(smem + L::o_ws);
   int* offs_s = reinterpret_cast<int*>(smem + L::o_offs);
   unsigned long long* mask_s = reinterpret_cast<unsigned long long*>(smem + L::o_mask);
-  int* tmp = reinterpret_cast<int*>(smem + L::o_tmp);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::o_mbar);
 
   int32_t* lid_all = reinterpret_cast<int32_t*>(smem + L::o_lid);
@@ -119,7 +115,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   // memory: arrive now (relaxed: nothing to publish, and no wait for the copies in
   // flight), wait after routing
   for (int e = tid; e < a.NE; e += kDecodeThreads) mask_s[e] = 0ull;
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  if (nctas > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   // launched as a programmatic dependent: everything above overlaps the preceding
   // kernel; inputs are read and outputs written only after it has completed
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -155,7 +151,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
       lid_all[t * kMaxK + lane] = o.lid;
     }
   }
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (nctas > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   // ---- a9..a11: this warp's row of ids goes to every other CTA, 16 bytes per store
   if (w < nrows) {
     __syncwarp();
@@ -176,7 +172,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
                    : "memory");
     }
   }
-  cluster.sync();  // release the stores above, acquire every other CTA's
+  // release the stores above, acquire every other CTA's (one CTA: a block barrier)
+  if (nctas > 1) cluster.sync();
+  else __syncthreads();
   uint32_t* mask32 = reinterpret_cast<uint32_t*>(mask_s);
   for (int x = tid; x < a.T * a.k; x += kDecodeThreads) {
     const int t = x / a.k, j = x - t * a.k;
@@ -185,7 +183,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   }
   __syncthreads();
 
-  mask_count_scan(mask_s, offs_s, a.NE, tmp);
+  mask_count_scan(mask_s, offs_s, a.NE);
   if (crank == 0) {
     for (int e = tid; e < a.NE; e += kDecodeThreads) {
       a.counts[e] = __popcll(mask_s[e]);
