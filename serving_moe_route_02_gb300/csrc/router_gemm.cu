@@ -120,6 +120,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* done = empty + kMaxStages;
   uint64_t* recv_bar = done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
+  // the 2^(j/64) table of the epilogue's score function, staged once (512 bytes)
+  float2* etab_s = reinterpret_cast<float2*>(recv_bar + 2);
+  if (threadIdx.x < kExpTable) etab_s[threadIdx.x] = g.etab[threadIdx.x];
   float* stage_rows = reinterpret_cast<float*>(stages);  // [128][kRowPad], reuses the ring
   const int kb0 = r * g.kb_per_cta;
   const uint32_t stage_bytes = uint32_t(kStageW + g.Tpad * kBK * 2);
@@ -248,21 +251,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // ---- this CTA's R experts: sum the C partial rows in source order, float4 stores
   const bool recv_ok = mbar_wait_bounded(recv_bar, 0, g.err);
   if (recv_ok) {
-    const int ngrp = R / 4;
-    for (int idx = threadIdx.x; idx < ngrp * g.T; idx += kGemmThreads) {
-      const int t = idx % g.T, i0 = (idx / g.T) * 4;
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      for (int c = 0; c < C; ++c) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], recv[(c * R + i0 + q) * rs + t]);
+    if (R * g.T <= kGemmThreads) {
+      // few tokens: one (expert, token) pair per thread, shortest chain
+      const int idx = threadIdx.x;
+      if (idx < R * g.T) {
+        const int t = idx % g.T, i = idx / g.T;
+        float acc = 0.0f;
+#pragma unroll 8
+        for (int c = 0; c < C; ++c) acc = __fadd_rn(acc, recv[(c * R + i) * rs + t]);
+        const int e = mtile * kBM + r * R + i;
+        if (g.logits) g.logits[size_t(t) * g.E + e] = acc;
+        g.scores[size_t(t) * g.E + e] = sig_f32(acc, etab_s);
       }
-      const int e = mtile * kBM + r * R + i0;
-      if (g.logits)
-        *reinterpret_cast<float4*>(g.logits + size_t(t) * g.E + e) =
-            make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(g.scores + size_t(t) * g.E + e) =
-          make_float4(sig_f32(acc[0], g.etab), sig_f32(acc[1], g.etab), sig_f32(acc[2], g.etab),
-                      sig_f32(acc[3], g.etab));
+    } else {
+      const int ngrp = R / 4;
+      for (int idx = threadIdx.x; idx < ngrp * g.T; idx += kGemmThreads) {
+        const int t = idx % g.T, i0 = (idx / g.T) * 4;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int c = 0; c < C; ++c) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], recv[(c * R + i0 + q) * rs + t]);
+        }
+        const int e = mtile * kBM + r * R + i0;
+        if (g.logits)
+          *reinterpret_cast<float4*>(g.logits + size_t(t) * g.E + e) =
+              make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(g.scores + size_t(t) * g.E + e) =
+            make_float4(sig_f32(acc[0], etab_s), sig_f32(acc[1], etab_s), sig_f32(acc[2], etab_s),
+                        sig_f32(acc[3], etab_s));
+      }
     }
   }
   if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -291,7 +309,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
          CUDA_SUCCESS;
 }
 
-constexpr int kGemmSmem = kMaxStages * kStage + kRecvBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kGemmSmem = kMaxStages * kStage + kRecvBytes + 1024 /*align*/ + 256 /*barriers*/ +
+                          kExpTable * 8 /*score table*/;
 static_assert(kMaxStages * kStage >= kBM * kRowPad * 4, "staged rows must fit the ring");
 static_assert(kGemmSmem <= 227 * 1024, "router contraction smem exceeds 227 KB");
 
