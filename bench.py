@@ -331,8 +331,22 @@ def layout_timing(torch, mr, dev, out, T, tile=128, reps=50):
 
 
 def run_case(torch, mr, dev, args, T=64):
-    """Plain launches of one decode-size path, for ncu captures."""
-    if args.case == "decode":
+    """Plain launches of one path, for ncu captures: decode routing or contraction +
+    routing at 64 rows, or the expert-GEMM layout / the index of packed ids at 65,536
+    rows (global ids, tile 128)."""
+    if args.case in ("layout", "index"):
+        cfg = gen.cfg3(T_PREFILL)
+        lg = to_dev_bf16(torch, cfg["logits"], dev)
+        bias = torch.from_numpy(cfg["bias"]).to(dev)
+        out = mr.route(lg, bias)
+        if args.case == "layout":
+            L = mr.route_layout(out, 128)
+            step = lambda: mr.route_layout(out, 128, layout=L)  # noqa: E731
+        else:
+            idx = mr.route_index(out["packed"], E)
+            step = lambda: mr.route_index(out["packed"], E, out=idx)  # noqa: E731
+        T = T_PREFILL
+    elif args.case == "decode":
         cfg = gen.cfg1(T)
         lg = to_dev_bf16(torch, cfg["logits"], dev)
         bias = torch.from_numpy(cfg["bias"]).to(dev)
@@ -371,10 +385,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--case", default=None, choices=["decode", "gemm"],
-                    help="run only --steps plain launches of one path (decode routing at 64 "
-                         "rows, or contraction + routing at 64 rows) and print a one-line "
-                         "summary: the commands profiled under ncu")
+    ap.add_argument("--case", default=None, choices=["decode", "gemm", "layout", "index"],
+                    help="run only --steps plain launches of one path (decode routing or "
+                         "contraction + routing at 64 rows, expert-GEMM layout or index of "
+                         "packed ids at 65,536 rows) and print a one-line summary: the "
+                         "commands profiled under ncu")
     ap.add_argument("--quick", action="store_true",
                     help="timed prefill steps only (no decode sweep, CPU baseline, end-to-end or "
                          "clock probe): the command profiled under ncu")

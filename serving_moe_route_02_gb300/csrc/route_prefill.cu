@@ -81,6 +81,14 @@ static_assert(PrefillSmem<DT_BF16, true>::LID_ENTRIES >= 512 && PrefillSmem<DT_B
 static_assert(PrefillSmem<DT_BF16, true>::ROWB % 128 == 0 && PrefillSmem<DT_F32, true>::ROWB % 128 == 0,
               "row slots keep 128-byte alignment");
 
+// Index mode: true in the lanes of kmask whose id appears more than once among the
+// row's k ids held by lanes 0..k-1 (all lanes of kmask must call it).
+__device__ __forceinline__ bool repeated_in_row(int l, unsigned kmask, int k) {
+  int n = 0;
+  for (int j = 0; j < k; ++j) n += __shfl_sync(kmask, l, j) == l;
+  return n > 1;
+}
+
 // Grid-wide barrier for a cooperative launch, bounded in time.  One arrival counter:
 // CTA 0 adds 2^31 - (nblocks - 1), every other CTA adds 1, so the counter's top bit
 // flips exactly when all have arrived (it starts at 0 and every completed barrier
@@ -200,6 +208,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   }
   for (int e = tid; e < a.NE; e += NT) hist_s[e] = 0;
   __syncthreads();
+  const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
   if constexpr (L::INDEX) {
     // ---- phase 1 (index mode): count this warp's given packed ids, 8 rows of loads in
     //      flight; an id at or above the bin count is reported and left out
@@ -210,17 +219,16 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         v[q] = (i0 + q < nw && lane < a.k) ? pk[size_t(wr0 + i0 + q) * a.k + lane] : 0;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        if (i0 + q < nw) {
-          // ids must be distinct within a row: a repeated id is reported and left out
-          // here and in phase 3 alike
-          const int l = (lane < a.k) ? int(uint32_t(v[q]) >> 16) : -1 - lane;
-          const bool repeated = __popc(__match_any_sync(0xffffffffu, l)) > 1;
-          if (lane < a.k && (i0 + q) * a.k + lane < L::LID_ENTRIES)
-            lid16[(i0 + q) * a.k + lane] = static_cast<uint16_t>(l);
-          if (lane < a.k) {
-            if (l < a.NE && !repeated) atomicAdd(&hist_s[l], 1);
-            else atomicExch(a.err, kErrBadId);
-          }
+        if (i0 + q < nw && lane < a.k) {
+          // ids must be distinct within a row: an id >= NE or repeated is reported and
+          // left out here and in phase 3 alike (kept as 0xFFFF, never a bin)
+          const int l = int(uint32_t(v[q]) >> 16);
+          const bool rep = repeated_in_row(l, kmask, a.k);  // every lane of kmask, always
+          const bool bad = l >= a.NE || rep;
+          if ((i0 + q) * a.k + lane < L::LID_ENTRIES)
+            lid16[(i0 + q) * a.k + lane] = static_cast<uint16_t>(bad ? 0xFFFF : l);
+          if (!bad) atomicAdd(&hist_s[l], 1);
+          else atomicExch(a.err, kErrBadId);
         }
       }
     }
@@ -345,7 +353,6 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   auto lid_of = [&](int c0, int r) -> int {
     return keep ? int(lid16[(c0 + r) * a.k + lane]) : int(uint32_t(stage[r * a.k + lane]) >> 16);
   };
-  const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
   auto stage_chunk = [&](int c0) {
     const int n = min(chunk_rows, nw - c0) * a.k;
     const int32_t* src = pk + size_t(wr0 + c0) * a.k;
@@ -376,9 +383,10 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         const int l = lid_of(c0, r);
         bool use = true;
         if constexpr (L::INDEX) {
-          // every lane of kmask takes part in the match, whatever its id
-          const unsigned same = __match_any_sync(kmask, l);
-          use = l < a.NE && __popc(same) == 1;
+          // kept ids carry phase 1's verdict; staged ones are checked again
+          // (keep is the same in every lane: either all lanes of kmask shuffle or none)
+          const bool rep = keep ? false : repeated_in_row(l, kmask, a.k);
+          use = l < a.NE && !rep;
         }
         if (use) atomicAdd(&wpre[l], 1);
       }
@@ -414,9 +422,10 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         const int l = lid_of(c0, r);
         bool use = true;
         if constexpr (L::INDEX) {
-          // every lane of kmask takes part in the match, whatever its id
-          const unsigned same = __match_any_sync(kmask, l);
-          use = l < a.NE && __popc(same) == 1;
+          // kept ids carry phase 1's verdict; staged ones are checked again
+          // (keep is the same in every lane: either all lanes of kmask shuffle or none)
+          const bool rep = keep ? false : repeated_in_row(l, kmask, a.k);
+          use = l < a.NE && !rep;
         }
         if (use) {
           const int rk = wpre[l];
