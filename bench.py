@@ -478,31 +478,29 @@ def main():
               and torch.equal(torch.sort(o["perm"].long()).values,
                               torch.arange(T_PREFILL * K, device=dev)))
 
-    # end to end: pinned host logits -> device -> route -> outputs back to pinned host
-    h_in = torch.from_numpy(host_logits.view(np.int16)).pin_memory()
-    h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()
-             if v is not None}
-    d_in = bufs[0]
+    # end to end through the host-buffer entry point: pinned host logits in, all outputs
+    # back to pinned host memory, every step (moe_route_host: the input copy of step
+    # i + 1 overlaps the routing and result copies of step i)
+    h_in = torch.from_numpy(host_logits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = mr.alloc_host_outputs(T_PREFILL, E, K, 0, want_ids=False)
     e2e_steps = 0 if args.quick else max(3, min(args.steps, 100))
     h2d = h_in.numel() * 2
-    d2h = sum(v.numel() * v.element_size() for v in h_out.values())
+    d2h = sum(v.numel() * v.element_size() for v in h_out.values() if v is not None)
     for _ in range(2 if e2e_steps else 0):
-        d_in.view(torch.int16).copy_(h_in, non_blocking=True)
-        mr.route(d_in, bias, out=outs[0])
-        for k2, v in h_out.items():
-            v.copy_(outs[0][k2], non_blocking=True)
+        mr.route_host(h_in, bias, out=h_out, synchronize=False)
     torch.cuda.synchronize()
     ea = torch.cuda.Event(enable_timing=True)
     eb = torch.cuda.Event(enable_timing=True)
     ea.record(stream)
+    stream.synchronize()  # the start stamp precedes the first input copy
     for _ in range(e2e_steps):
-        d_in.view(torch.int16).copy_(h_in, non_blocking=True)
-        mr.route(d_in, bias, out=outs[0])
-        for k2, v in h_out.items():
-            v.copy_(outs[0][k2], non_blocking=True)
+        mr.route_host(h_in, bias, out=h_out, synchronize=False)
     eb.record(stream)
     torch.cuda.synchronize()
     e2e_ms = ea.elapsed_time(eb) / max(1, e2e_steps)
+    if e2e_steps:  # the host results are the device path's
+        ok = ok and all(torch.equal(h_out[k2], outs[0][k2].cpu()) for k2 in ("packed", "counts", "offsets", "perm"))
+        ok = ok and mr.device_status() == 0
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -539,7 +537,9 @@ def main():
                      "kernel_us": kernel_ms * 1e3, "peak_source": f"{peak_src} hbm_gbs (copy)"},
         "clocks": clocks,
         "e2e": ({"value": world * T_PREFILL / (e2e_ms * 1e-3), "unit": "tokens/s",
-                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                 "api": "moe_route_host (host buffers; two device staging slots, so the input "
+                        "copy of step i + 1 overlaps step i)"}
                 if e2e_steps else None),
         "gpu_launches": args.steps,
         "device_status": status, "invariants_ok": ok,

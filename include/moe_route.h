@@ -261,6 +261,45 @@ int moe_route_noalloc(const void* logits, int logits_dtype, const float* bias, i
                       struct CUstream_st* stream);
 
 /*
+ * moe_route_host -- moe_route for a logit matrix in HOST memory, results to HOST memory.
+ * The pages describe no counterpart: this is the end-to-end form of the same routing
+ * (input transfer, the routing kernels, result transfer), not a step of the method.
+ *   logits            [T, E] float32 or bfloat16 bits in host memory (any alignment).
+ *   bias              [E] float32, DEVICE pointer, 16-byte aligned (a model parameter
+ *                     that stays resident).
+ *   packed, counts, offsets, perm, topk_ids   host memory, sizes as for moe_route
+ *                     (topk_ids nullable).
+ *   Other arguments, the results and the argument errors are those of moe_route.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister); then the call
+ * only enqueues work and returns, and the results are in place once `stream` has
+ * completed the work enqueued so far (cudaStreamSynchronize).  Pageable buffers work
+ * but make the copies synchronous with the host.
+ * The library copies the logits into one of two device staging slots per device
+ * (allocated on first use and grown with cudaMalloc; cudaFree when a slot grows),
+ * on its own copy stream, routes them on `stream` and copies the results back on
+ * `stream`.  Consecutive calls alternate between the slots, so call i + 1's input
+ * transfer runs while call i routes and returns its results.  Consequences:
+ *   - The logits are read at some point between the call and the completion of its
+ *     routing, possibly before work enqueued earlier on `stream` has run: they must be
+ *     complete when the call is made and unchanged until `stream` has finished the
+ *     call's work; they must not be the target of work still pending on `stream`.
+ *   - Calls on one device must come from one thread at a time or be serialised by the
+ *     caller, and must be ordered on the GPU like moe_route calls (same stream).
+ *   - Not capturable: during stream capture it returns MOE_ROUTE_E_UNSUPPORTED and
+ *     enqueues nothing.
+ *   - Argument errors enqueue nothing.  A CUDA error after the input copy has been
+ *     enqueued returns MOE_ROUTE_E_CUDA with that copy still enqueued.
+ */
+int moe_route_host(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+                   int n_group, int topk_group, float scale, int local_offset, int local_count,
+                   int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
+                   int32_t* topk_ids, struct CUstream_st* stream);
+
+/* Frees the current device's moe_route_host staging slots, after waiting for the work
+ * that uses them.  The next moe_route_host call allocates them again. */
+int moe_route_host_release(void);
+
+/*
  * Measurement helper: enqueues one launch of an empty kernel with the decode kernel's
  * launch shape (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 8).  Replayed in a
  * CUDA graph it gives the launch-latency floor that decode routing is compared with.

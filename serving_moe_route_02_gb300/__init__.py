@@ -50,6 +50,10 @@ def load(path: str | None = None):
     lib.moe_route.restype = I
     lib.moe_router_gemm_route.argtypes = [P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
     lib.moe_router_gemm_route.restype = I
+    lib.moe_route_host.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P]
+    lib.moe_route_host.restype = I
+    lib.moe_route_host_release.argtypes = []
+    lib.moe_route_host_release.restype = I
     lib.moe_route_bins.argtypes = [I, I, I]
     lib.moe_route_bins.restype = I
     lib.moe_route_num_experts.argtypes = [I, I, I, I]
@@ -161,6 +165,41 @@ def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int
                           _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]),
                           _ptr(out.get("ids")), _stream(stream))
     _check(rc, "moe_route")
+    return out
+
+
+def alloc_host_outputs(T: int, E: int, k: int = 16, local_count: int = 0,
+                       want_ids: bool = False) -> dict:
+    """Page-locked host output buffers for route_host."""
+    NE = load().moe_route_bins(E, k, local_count)
+    pin = dict(dtype=torch.int32, pin_memory=True)
+    out = {"packed": torch.empty((T, k), **pin), "counts": torch.empty(NE, **pin),
+           "offsets": torch.empty(NE + 1, **pin), "perm": torch.empty(T * k, **pin)}
+    out["ids"] = torch.empty((T, k), **pin) if want_ids else None
+    return out
+
+
+def route_host(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int = 8,
+               topk_group: int = 4, scale: float = 2.5, local_offset: int = 0, local_count: int = 0,
+               out: dict | None = None, want_ids: bool = False, stream=None,
+               synchronize: bool = True) -> dict:
+    """moe_route_host: a [T, E] CPU tensor of router logits (float32 or bfloat16; pinned
+    for asynchronous transfer), bias on the device, results in CPU tensors.  With
+    synchronize=False the results are valid once the stream has completed the call."""
+    if logits.is_cuda or not bias.is_cuda:
+        raise ValueError("logits must be a CPU tensor and bias a CUDA tensor")
+    if not logits.is_contiguous() or not bias.is_contiguous() or bias.dtype != torch.float32:
+        raise ValueError("logits and bias must be contiguous; bias float32")
+    T, E = logits.shape
+    if out is None:
+        out = alloc_host_outputs(T, E, k, local_count, want_ids)
+    rc = load().moe_route_host(_ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group,
+                               topk_group, float(scale), local_offset, local_count,
+                               _ptr(out["packed"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+                               _ptr(out["perm"]), _ptr(out.get("ids")), _stream(stream))
+    _check(rc, "moe_route_host")
+    if synchronize:
+        (stream or torch.cuda.current_stream()).synchronize()
     return out
 
 

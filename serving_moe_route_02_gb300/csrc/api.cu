@@ -110,6 +110,12 @@ int check_route_args(int T, int E, int k, int n_group, int topk_group, int off, 
 
 }  // namespace
 
+namespace moe {
+int route_args_status(int T, int E, int k, int n_group, int topk_group, int off, int cnt) {
+  return check_route_args(T, E, k, n_group, topk_group, off, cnt);
+}
+}  // namespace moe
+
 extern "C" {
 
 int moe_route_bins(int E, int k, int local_count) { return bins(E, k, local_count); }

@@ -50,6 +50,8 @@ cudaError_t setup_prefill_kernels(int* blocks_per_sm);
 // False when a warp of the persistent kernel would get 65,536 rows or more (its 16-bit
 // bin counters would overflow); the launcher then refuses the launch.
 bool prefill_fits(int T, int grid);
+// The argument checks of moe_route (status code; MOE_ROUTE_OK when the call is valid).
+int route_args_status(int T, int E, int k, int n_group, int topk_group, int off, int cnt);
 cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,
                                  cudaStream_t st);
 
