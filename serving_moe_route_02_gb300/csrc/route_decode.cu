@@ -52,28 +52,41 @@ static_assert(DecodeSmem<DT_PACKED>::total <= 227 * 1024, "decode smem (index) e
 static_assert(kDecodeRowsPerCta * kDecodeMaxCtas <= 64, "row masks are 64 bits");
 
 // Exclusive scan over the bins of counts popc(mask[e]) into offs[0..n], offs[n] = total,
-// by warp 0 alone (lane l takes a contiguous run of bins), then one block barrier.
+// by the whole block: thread i takes the bins [i per, i per + per), per = ceil(n / 256)
+// (at most 5), with all its mask loads in flight; warp scans, then the warp totals
+// through `wtot` (8 ints).  Ends with a block barrier.
 // mask[e] holds rows 0..31 in its low word, 32..63 in its high word.
-__device__ __forceinline__ void mask_count_scan(const unsigned long long* mask, int* offs, int n) {
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int per = (n + 31) / 32;
-    const int lo = min(n, lane * per), hi = min(n, lo + per);
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += __popcll(mask[i]);
-    int incl = sum;
+__device__ __forceinline__ void mask_count_scan(const unsigned long long* mask, int* offs, int n,
+                                                int* wtot) {
+  constexpr int kPer = (kMaxBins + kDecodeThreads - 1) / kDecodeThreads;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (n + kDecodeThreads - 1) / kDecodeThreads;
+  const int lo = tid * per;
+  int c[kPer];
+  int sum = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += u;
-    }
-    int run = incl - sum;
-    for (int i = lo; i < hi; ++i) {
-      offs[i] = run;
-      run += __popcll(mask[i]);
-    }
-    if (lane == 31) offs[n] = incl;
+  for (int q = 0; q < kPer; ++q) {
+    c[q] = (q < per && lo + q < n) ? __popcll(mask[lo + q]) : 0;
+    sum += c[q];
   }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) wtot[w] = incl;
+  __syncthreads();
+  int wpre = 0;
+#pragma unroll
+  for (int i = 0; i < kDecodeRowsPerCta; ++i) wpre += (i < w) ? wtot[i] : 0;
+  int run = wpre + incl - sum;
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    if (q < per && lo + q < n) offs[lo + q] = run;
+    run += c[q];
+  }
+  if (tid == kDecodeThreads - 1) offs[n] = run;
   __syncthreads();
 }
 
@@ -176,14 +189,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   if (nctas > 1) cluster.sync();
   else __syncthreads();
   uint32_t* mask32 = reinterpret_cast<uint32_t*>(mask_s);
-  for (int x = tid; x < a.T * a.k; x += kDecodeThreads) {
-    const int t = x / a.k, j = x - t * a.k;
+  const int kk = SPEC ? 16 : a.k;
+  for (int x = tid; x < a.T * kk; x += kDecodeThreads) {
+    const int t = x / kk, j = x - t * kk;
     const int l = lid_all[t * kMaxK + j];
     if (DT != DT_PACKED || l >= 0) atomicOr(mask32 + 2 * l + (t >> 5), 1u << (t & 31));
   }
   __syncthreads();
 
-  mask_count_scan(mask_s, offs_s, a.NE);
+  mask_count_scan(mask_s, offs_s, a.NE, reinterpret_cast<int*>(smem + L::o_tmp));
   if (crank == 0) {
     for (int e = tid; e < a.NE; e += kDecodeThreads) {
       a.counts[e] = __popcll(mask_s[e]);
