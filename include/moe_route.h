@@ -39,6 +39,12 @@
  *     zeroing is needed.
  *   - Calls on one device share one workspace: calls must be ordered on the GPU
  *     (same stream, or otherwise serialised); concurrent calls race.
+ *   - Routing of T <= 64 rows (and the routing behind moe_router_gemm_route) runs as
+ *     one kernel launched with programmatic stream serialization that signals its
+ *     dependents as it starts.  A kernel launched after it on the same stream WITH that
+ *     attribute may therefore start early and must execute griddepcontrol.wait
+ *     (cudaGridDependencySynchronize) before it reads the outputs; kernels launched
+ *     without it, and copies, start after the routing has completed, as usual.
  *   - Return value: MOE_ROUTE_OK or a negative moe_route_status.  A call that returns
  *     an error has enqueued nothing.  Errors detected on the device (a bounded wait
  *     that ran out) are reported by moe_route_device_status().
@@ -301,7 +307,8 @@ int moe_route_host_release(void);
 
 /*
  * Measurement helper: enqueues one launch of an empty kernel with the decode kernel's
- * launch shape (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 8).  Replayed in a
+ * launch shape and attributes (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 8,
+ * programmatic stream serialization).  Replayed in a
  * CUDA graph it gives the launch-latency floor that decode routing is compared with.
  */
 int moe_route_empty(int ctas, struct CUstream_st* stream);

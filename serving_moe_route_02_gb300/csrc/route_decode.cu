@@ -113,6 +113,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   const uint32_t bytes = uint32_t(nrows) * L::ROWB + uint32_t(L::STAB) + uint32_t(L::BIASB);
   const bool have = DT != DT_PACKED && nrows > 0;  // CTAs without rows (T = 0) load nothing
 
+  // a programmatic dependent launched after this kernel (the next routing call) may
+  // start now: before its own griddepcontrol.wait it only loads the constant score
+  // table, and that wait returns once this grid has completed and its writes are visible
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     mbar_init(mbar, 1);
     fence_mbar_init();
@@ -261,13 +265,15 @@ cudaError_t launch_empty(int ctas, cudaStream_t st) {
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = ctas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // as the routing kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_empty);
 }
 
