@@ -218,14 +218,14 @@ def to_dev_bf16(torch, arr, dev):
 def decode_latency(torch, mr, dev, reps=200, replays=10):
     """µs per call under CUDA-graph replay (rank-local ids, offset 336, count 112),
     against an empty kernel with the same launch shape replayed the same way."""
-    res = {"T": [], "us_per_call": [], "floor_us": [], "ratio_to_floor": []}
+    res = {"T": [], "ctas": [], "us_per_call": [], "floor_us": [], "ratio_to_floor": []}
     st = torch.cuda.Stream(device=dev)
     for T in (8, 16, 24, 32, 64):
         cfg = gen.cfg1(T)
         lg = to_dev_bf16(torch, cfg["logits"], dev)
         bias = torch.from_numpy(cfg["bias"]).to(dev)
         out = mr.alloc_outputs(T, E, K, 112, dev)
-        ctas = (T + 7) // 8
+        ctas = mr.decode_ctas(T)  # the routing launch's cluster
         with torch.cuda.stream(st):
             mr.route(lg, bias, local_offset=336, local_count=112, out=out, stream=st)
             mr.empty_kernel(ctas, stream=st)
@@ -254,6 +254,7 @@ def decode_latency(torch, mr, dev, reps=200, replays=10):
                     samples.append(a.elapsed_time(b) * 1e3 / reps)
             times[name] = statistics.median(samples)
         res["T"].append(T)
+        res["ctas"].append(ctas)
         res["us_per_call"].append(round(times["route"], 3))
         res["floor_us"].append(round(times["empty"], 3))
         res["ratio_to_floor"].append(round(times["route"] / times["empty"], 3))

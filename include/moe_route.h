@@ -307,11 +307,19 @@ int moe_route_host_release(void);
 
 /*
  * Measurement helper: enqueues one launch of an empty kernel with the decode kernel's
- * launch shape and attributes (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 8,
- * programmatic stream serialization).  Replayed in a
+ * launch shape and attributes (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 16,
+ * programmatic stream serialization); moe_route_decode_ctas(T) gives the shape of a
+ * T-row routing launch.  A cluster of more than 8 CTAs may be refused (MOE_ROUTE_E_CUDA)
+ * on a GPU that cannot schedule it; the library's own launches never ask for one there.  Replayed in a
  * CUDA graph it gives the launch-latency floor that decode routing is compared with.
  */
 int moe_route_empty(int ctas, struct CUstream_st* stream);
+
+/* CTAs (one thread-block cluster) of the routing kernel for T <= 64 rows: 1 for T <= 8;
+ * otherwise the fewest that hold max(2, ceil(T / M)) rows each, M = 16 where the GPU can
+ * schedule clusters of 16 CTAs (else 8).  Creates the device state like
+ * moe_route_reserve.  INVALID_ARG for T outside [0, 64]. */
+int moe_route_decode_ctas(int T);
 
 /* Static description of a status code. */
 const char* moe_route_strerror(int status);

@@ -54,6 +54,8 @@ def load(path: str | None = None):
     lib.moe_route_host.restype = I
     lib.moe_route_host_release.argtypes = []
     lib.moe_route_host_release.restype = I
+    lib.moe_route_decode_ctas.argtypes = [I]
+    lib.moe_route_decode_ctas.restype = I
     lib.moe_route_bins.argtypes = [I, I, I]
     lib.moe_route_bins.restype = I
     lib.moe_route_num_experts.argtypes = [I, I, I, I]
@@ -106,6 +108,14 @@ def _ptr(t):
 def _stream(stream):
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def decode_ctas(T: int) -> int:
+    """CTAs of the routing kernel's launch for T <= 64 rows."""
+    n = load().moe_route_decode_ctas(T)
+    if n < 0:
+        raise MoeRouteError(n, "moe_route_decode_ctas")
+    return n
 
 
 def bins(E: int, k: int, local_count: int) -> int:

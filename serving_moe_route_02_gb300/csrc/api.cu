@@ -356,8 +356,16 @@ int moe_route_set_path(int path) {
   return prev;
 }
 
+int moe_route_decode_ctas(int T) {
+  if (T < 0 || T > 64) return MOE_ROUTE_E_INVALID_ARG;
+  DevState* d = nullptr;
+  const int rc = get_state(nullptr, &d);
+  if (rc != MOE_ROUTE_OK) return rc;
+  return decode_ctas(T);
+}
+
 int moe_route_empty(int ctas, struct CUstream_st* stream) {
-  if (ctas < 1 || ctas > 8) return MOE_ROUTE_E_INVALID_ARG;
+  if (ctas < 1 || ctas > 16) return MOE_ROUTE_E_INVALID_ARG;
   return launch_empty(ctas, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_ROUTE_OK
                                                                                      : MOE_ROUTE_E_CUDA;
 }

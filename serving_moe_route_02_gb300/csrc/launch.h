@@ -40,6 +40,7 @@ cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const flo
                            int n, cudaStream_t st);
 cudaError_t setup_decode_kernels();
 cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st);
+int decode_ctas(int T);  // CTAs (one cluster) of a decode launch of T <= 64 rows
 cudaError_t launch_empty(int ctas, cudaStream_t st);
 cudaError_t setup_router_gemm();
 int router_gemm_cluster();

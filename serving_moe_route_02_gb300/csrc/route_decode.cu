@@ -24,7 +24,8 @@ namespace moe {
 
 constexpr int kDecodeRowsPerCta = 8;
 constexpr int kDecodeThreads = 32 * kDecodeRowsPerCta;
-constexpr int kDecodeMaxCtas = 8;
+constexpr int kDecodeMaxCtas = 16;  // clusters of 16 where the GPU schedules them, else 8
+int g_decode_max_ctas = 8;
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
@@ -49,7 +50,7 @@ static_assert(DecodeSmem<DT_F32>::total <= 227 * 1024, "decode smem (f32) exceed
 static_assert(DecodeSmem<DT_BF16>::total <= 227 * 1024, "decode smem (bf16) exceeds 227 KB");
 static_assert(DecodeSmem<DT_SCORE>::total <= 227 * 1024, "decode smem (scores) exceeds 227 KB");
 static_assert(DecodeSmem<DT_PACKED>::total <= 227 * 1024, "decode smem (index) exceeds 227 KB");
-static_assert(kDecodeRowsPerCta * kDecodeMaxCtas <= 64, "row masks are 64 bits");
+// row masks are 64 bits: the launcher takes at most 64 rows
 
 // Exclusive scan over the bins of counts popc(mask[e]) into offs[0..n], offs[n] = total,
 // by the whole block: thread i takes the bins [i per, i per + per), per = ceil(n / 256)
@@ -108,8 +109,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int crank = static_cast<int>(cluster.block_rank());
   const int nctas = static_cast<int>(cluster.num_blocks());
-  const int row0 = crank * kDecodeRowsPerCta;
-  const int nrows = max(0, min(kDecodeRowsPerCta, a.T - row0));
+  // rows split evenly over the cluster's CTAs (at most 8 each), so that for 9..63 rows
+  // fewer warps share an SM's shared-memory bandwidth in the score phase
+  const int rpc = (a.T + nctas - 1) / nctas;
+  const int row0 = crank * rpc;
+  const int nrows = max(0, min(rpc, a.T - row0));
   const uint32_t bytes = uint32_t(nrows) * L::ROWB + uint32_t(L::STAB) + uint32_t(L::BIASB);
   const bool have = DT != DT_PACKED && nrows > 0;  // CTAs without rows (T = 0) load nothing
 
@@ -258,6 +262,15 @@ cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const flo
   return cudaGetLastError();
 }
 
+// CTAs of a decode launch: one for up to 8 rows (no cluster barrier); above that, the
+// fewest CTAs that hold max(2, ceil(T / M)) rows each, M = 16 where clusters of 16 can
+// be scheduled, else 8 (64 rows: 16 CTAs of 4 rows, or 8 of 8).
+int decode_ctas(int T) {
+  if (T <= kDecodeRowsPerCta) return 1;
+  const int per = max(2, (T + g_decode_max_ctas - 1) / g_decode_max_ctas);
+  return (T + per - 1) / per;
+}
+
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_empty() {}
 
 cudaError_t launch_empty(int ctas, cudaStream_t st) {
@@ -277,21 +290,54 @@ cudaError_t launch_empty(int ctas, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, k_empty);
 }
 
+// Shared-memory size of one decode kernel; clears *wide if clusters of 16 are refused.
 template <int DT, bool SPEC>
-static cudaError_t set_decode_smem() {
-  return cudaFuncSetAttribute(k_route_decode<DT, SPEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              DecodeSmem<DT>::total);
+static cudaError_t set_decode_smem(bool* wide) {
+  cudaError_t e = cudaFuncSetAttribute(k_route_decode<DT, SPEC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, DecodeSmem<DT>::total);
+  if (e != cudaSuccess) return e;
+  if (cudaFuncSetAttribute(k_route_decode<DT, SPEC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    *wide = false;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t setup_decode_kernels() {
   cudaError_t e;
-  if ((e = set_decode_smem<DT_F32, false>()) != cudaSuccess) return e;
-  if ((e = set_decode_smem<DT_F32, true>()) != cudaSuccess) return e;
-  if ((e = set_decode_smem<DT_BF16, false>()) != cudaSuccess) return e;
-  if ((e = set_decode_smem<DT_BF16, true>()) != cudaSuccess) return e;
-  if ((e = set_decode_smem<DT_SCORE, false>()) != cudaSuccess) return e;
-  if ((e = set_decode_smem<DT_PACKED, false>()) != cudaSuccess) return e;
-  return set_decode_smem<DT_SCORE, true>();
+  bool wide = true;
+  if ((e = set_decode_smem<DT_F32, false>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_F32, true>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_BF16, false>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_BF16, true>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_SCORE, false>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_SCORE, true>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_PACKED, false>(&wide)) != cudaSuccess) return e;
+  if (cudaFuncSetAttribute(k_empty, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    wide = false;
+  }
+  g_decode_max_ctas = wide ? 16 : 8;
+  // clusters of 16 only where one can be resident (the largest shared-memory variant)
+  if (g_decode_max_ctas == 16) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(kDecodeThreads, 1, 1);
+    cfg.dynamicSmemBytes = DecodeSmem<DT_BF16>::total;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_route_decode<DT_BF16, true>, &cfg) != cudaSuccess || n < 1)
+      g_decode_max_ctas = 8;
+    cudaGetLastError();  // clear a refused query
+  }
+  return cudaSuccess;
 }
 
 template <int DT, bool SPEC>
@@ -301,8 +347,8 @@ static cudaError_t launch_decode_t(cudaLaunchConfig_t& cfg, const RouteArgs& a) 
 }
 
 cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) {
-  const int ctas = max(1, (a.T + kDecodeRowsPerCta - 1) / kDecodeRowsPerCta);
-  if (ctas > kDecodeMaxCtas) return cudaErrorInvalidValue;
+  if (a.T > kDecodeRowsPerCta * kDecodeMaxCtas) return cudaErrorInvalidValue;
+  const int ctas = decode_ctas(a.T);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);

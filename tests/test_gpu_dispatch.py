@@ -25,7 +25,7 @@ def routed(mr, cfg):
                     local_count=cfg["cnt"], want_ids=True)
 
 
-@pytest.mark.parametrize("T,off,cnt", [(1, 0, 0), (8, 336, 112), (64, 0, 0), (65, 784, 112),
+@pytest.mark.parametrize("T,off,cnt", [(1, 0, 0), (8, 336, 112), (17, 0, 0), (50, 336, 112), (64, 0, 0), (65, 784, 112),
                                        (1001, 0, 0), (16384, 784, 112), (65536, 0, 0)])
 def test_index_of_routed_packed(mr, T, off, cnt):
     """Indexing the routing's own packed ids gives the routing's counts, offsets, perm
