@@ -298,35 +298,47 @@ def gemm_route_latency(torch, mr, dev, reps=100, replays=10):
     return res
 
 
-def layout_timing(torch, mr, dev, out, T, tile=128, reps=50):
-    """moe_route_layout at T rows (global ids, one call per step): µs per call and the
-    HBM bandwidth of its algorithmic bytes (perm read once, inverse written, padded rows
-    and m_indices written over the whole capacity)."""
+def layout_timing(torch, mr, dev, out, T, tile=128, reps=50, replays=10):
+    """moe_route_layout at T rows (global ids): µs per call under CUDA-graph replay (so
+    that host-side call overhead does not hide the kernel), with and without the inverse
+    permutation, and the HBM bandwidth of its algorithmic bytes (perm read once, inverse
+    written, padded rows and m_indices written over the whole capacity)."""
     L = mr.route_layout(out, tile)
     torch.cuda.synchronize()
     n = T * K
     NE = out["counts"].numel()
     cap = L["padded_rows"].numel()
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        mr.route_layout(out, tile, layout=L)
-    b.record()
-    torch.cuda.synchronize()
-    us = a.elapsed_time(b) * 1e3 / reps
-    Lp = dict(L, inv_perm=None)
-    a.record()
-    for _ in range(reps):
-        mr.route_layout(out, tile, layout=Lp)
-    b.record()
-    torch.cuda.synchronize()
-    us_padded = a.elapsed_time(b) * 1e3 / reps
+    st = torch.cuda.Stream(device=dev)
+
+    def replay_us(layout):
+        with torch.cuda.stream(st):
+            st.wait_stream(torch.cuda.current_stream(dev))
+            mr.route_layout(out, tile, layout=layout, stream=st)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for _ in range(reps):
+                    mr.route_layout(out, tile, layout=layout, stream=st)
+            g.replay()
+            st.synchronize()
+            samples = []
+            for _ in range(replays):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                g.replay()
+                b.record(st)
+                b.synchronize()
+                samples.append(a.elapsed_time(b) * 1e3 / reps)
+        return statistics.median(samples)
+
+    us = replay_us(L)
+    us_padded = replay_us(dict(L, inv_perm=None))
     nbytes = 4 * n + 4 * n + 2 * 4 * cap + 4 * (2 * NE + 1) + 4 * (NE + 1)
     peaks, _ = measured_peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"T": T, "tile": tile, "capacity": cap, "us_per_call": round(us, 3),
-            "us_per_call_without_inverse": round(us_padded, 3),
+            "us_per_call_without_inverse": round(us_padded, 3), "timing": "CUDA-graph replay",
             "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
             "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
 
