@@ -262,11 +262,12 @@ cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const flo
   return cudaGetLastError();
 }
 
-// CTAs of a decode launch: one for up to 8 rows (no cluster barrier); above that, the
-// fewest CTAs that hold max(2, ceil(T / M)) rows each, M = 16 where clusters of 16 can
-// be scheduled, else 8 (64 rows: 16 CTAs of 4 rows, or 8 of 8).
+// CTAs of a decode launch: one for up to 5 rows (no cluster barrier, which costs about
+// 0.3 us); above that, the fewest CTAs that hold max(2, ceil(T / M)) rows each, M = 16
+// where clusters of 16 can be scheduled, else 8 (8 rows: 4 CTAs of 2; 64 rows: 16 CTAs
+// of 4, or 8 of 8).  Measured crossover: 6 rows.
 int decode_ctas(int T) {
-  if (T <= kDecodeRowsPerCta) return 1;
+  if (T <= 5) return 1;
   const int per = max(2, (T + g_decode_max_ctas - 1) / g_decode_max_ctas);
   return (T + per - 1) / per;
 }

@@ -89,7 +89,7 @@ def test_cfg0_smallest(mr):
     check(mr, gen.cfg0(), exact=False)
 
 
-@pytest.mark.parametrize("T", [8, 9, 16, 17, 24, 32, 41, 57, 63, 64])  # 1..8 CTAs, ragged splits
+@pytest.mark.parametrize("T", [5, 6, 7, 8, 9, 16, 17, 24, 32, 41, 57, 63, 64])  # 1..16 CTAs, ragged splits
 @pytest.mark.parametrize("local", [True, False])
 def test_cfg1_decode_sweep(mr, T, local):
     cfg = gen.cfg1(T) if local else gen.cfg1(T, off=0, cnt=0)
