@@ -108,6 +108,11 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
  *   1 <= T <= 64 (decode batches).
  *   logits_out  [T, E] float32 out, nullable (the fp32 logits the routing used).
  *   other arguments as moe_route.  Supported: E = 896, n_group = 8, H % 64 == 0.
+ * w_router is read as a constant model weight: the contraction kernel is launched as a
+ * programmatic dependent and starts loading the weight before the preceding kernel on
+ * `stream` has completed (hidden, bias and all outputs wait for it).  The weight must
+ * therefore not be written by work still pending on `stream` when the call is made
+ * (write it, then synchronise, before the first call that reads it).
  */
 int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, const float* bias,
                           int T, int H, int E, int k, int n_group, int topk_group, float scale,

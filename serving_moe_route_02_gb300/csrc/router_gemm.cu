@@ -140,12 +140,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(done, 1);
     mbar_init(recv_bar, 1);
     fence_mbar_init();
+    // the weight is read as a constant: its loads start before the preceding kernel on
+    // the stream has completed (this grid is a programmatic dependent); the hidden rows
+    // follow after griddepcontrol.wait below, counted on the same stage barriers
     for (int kb = 0; kb < NS && kb < g.kb_per_cta; ++kb) {
       uint8_t* st = stages + kb * kStage;
       mbar_expect_tx(full + kb, stage_bytes);
-      const int k = (kb0 + kb) * kBK;
-      tma_load_2d(smem_addr(st), &tmW, k, mtile * kBM, smem_addr(full + kb));
-      tma_load_2d(smem_addr(st + kStageW), &tmH, k, 0, smem_addr(full + kb));
+      tma_load_2d(smem_addr(st), &tmW, (kb0 + kb) * kBK, mtile * kBM, smem_addr(full + kb));
     }
   }
   if (warp == 1) {
@@ -163,8 +164,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
+  // the hidden rows (and every output) depend on the preceding kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (threadIdx.x == 0) {
+    for (int kb = 0; kb < NS && kb < g.kb_per_cta; ++kb)
+      tma_load_2d(smem_addr(stages + kb * kStage + kStageW), &tmH, (kb0 + kb) * kBK, 0,
+                  smem_addr(full + kb));
     mbar_expect_tx(recv_bar, copy_bytes * uint32_t(C));  // C partial blocks will arrive
     // producer: refill stages freed by the MMAs (only when the K slice exceeds the ring)
     for (int kb = NS; kb < g.kb_per_cta; ++kb) {
@@ -396,13 +402,15 @@ cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float*
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = kGemmSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, k_router_gemm, tmW, tmH, g);
 }
 
