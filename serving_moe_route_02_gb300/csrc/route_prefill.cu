@@ -211,7 +211,16 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   const unsigned kmask = (a.k == 32) ? 0xffffffffu : ((1u << a.k) - 1u);
   if constexpr (L::INDEX) {
     // ---- phase 1 (index mode): count this warp's given packed ids, 8 rows of loads in
-    //      flight; an id at or above the bin count is reported and left out
+    //      flight.  Ids must be distinct within a row: an id >= NE, and every occurrence
+    //      of an id that appears twice in its row, is reported and left out here and in
+    //      phase 3 alike (kept as 0xFFFF, never a bin).  Repeats are found with two
+    //      bitmaps of the row's ids in the warp's (otherwise unused) ring slot: ids seen,
+    //      and ids seen twice; both are cleared after each row.
+    constexpr int kWords = kMaxBins / 32;
+    uint32_t* seen = reinterpret_cast<uint32_t*>(ring);
+    uint32_t* twice = seen + kWords;
+    for (int i = lane; i < 2 * kWords; i += 32) seen[i] = 0u;
+    __syncwarp();
     for (int i0 = 0; i0 < nw; i0 += 8) {
       int32_t v[8];
 #pragma unroll
@@ -219,17 +228,26 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         v[q] = (i0 + q < nw && lane < a.k) ? pk[size_t(wr0 + i0 + q) * a.k + lane] : 0;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        if (i0 + q < nw && lane < a.k) {
-          // ids must be distinct within a row: an id >= NE or repeated is reported and
-          // left out here and in phase 3 alike (kept as 0xFFFF, never a bin)
-          const int l = int(uint32_t(v[q]) >> 16);
-          const bool rep = repeated_in_row(l, kmask, a.k);  // every lane of kmask, always
-          const bool bad = l >= a.NE || rep;
+        const bool act = i0 + q < nw && lane < a.k;
+        const int l = act ? int(uint32_t(v[q]) >> 16) : 0;
+        const bool inb = act && l < a.NE;
+        const int wd = inb ? (l >> 5) : 0;  // bitmap word, in range on every lane
+        const uint32_t bit = 1u << (l & 31);
+        if (inb && (atomicOr(&seen[wd], bit) & bit) != 0u) atomicOr(&twice[wd], bit);
+        __syncwarp();
+        const bool bad = act && (!inb || (twice[wd] & bit) != 0u);
+        if (act) {
           if ((i0 + q) * a.k + lane < L::LID_ENTRIES)
             lid16[(i0 + q) * a.k + lane] = static_cast<uint16_t>(bad ? 0xFFFF : l);
           if (!bad) atomicAdd(&hist_s[l], 1);
           else atomicExch(a.err, kErrBadId);
         }
+        __syncwarp();  // every lane has read `twice` before the clear
+        if (inb) {
+          seen[wd] = 0u;
+          twice[wd] = 0u;
+        }
+        __syncwarp();
       }
     }
   } else {
