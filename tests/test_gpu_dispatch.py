@@ -79,6 +79,34 @@ def test_index_reports_bad_id(mr, T, fault):
     assert int(idx["counts"].sum()) <= T * 4
 
 
+@pytest.mark.parametrize("T", [16, 5000])
+def test_index_leaves_out_every_bad_entry(mr, T):
+    """Rows with an id repeated three times, a repeated pair and an id >= NE: both kernels
+    leave out exactly those entries (every occurrence of a repeated id), so the counts
+    are the histogram of the remaining ones and the permutation holds exactly them."""
+    k, NE = 8, 40
+    ids = distinct_rows(T, k, NE, 4200 + T)
+    bad_rows = sorted({1, T // 3, T // 2, T - 1})
+    ids[bad_rows[0], 2] = ids[bad_rows[0], 5] = ids[bad_rows[0], 0]   # three times
+    ids[bad_rows[1], 7] = ids[bad_rows[1], 3]                         # a pair
+    ids[bad_rows[2], 4] = NE + 3                                      # out of range
+    ids[bad_rows[3], 1] = ids[bad_rows[3], 6]
+    ids[bad_rows[3], 0] = NE
+    packed = ((ids << 16) | 0x3E20).astype(np.int32)
+    idx = mr.route_index(torch.from_numpy(packed).cuda(), NE)
+    assert mr.device_status() == mr.E_BAD_ID
+    valid = ids < NE
+    for t in range(T):
+        u, c = np.unique(ids[t], return_counts=True)
+        valid[t] &= ~np.isin(ids[t], u[c > 1])
+    flat = np.flatnonzero(valid.ravel())
+    assert np.array_equal(idx["counts"].cpu().numpy(), np.bincount(ids.ravel()[flat], minlength=NE))
+    n = len(flat)
+    assert int(idx["offsets"][-1]) == n
+    got = np.sort(idx["perm"].cpu().numpy()[:n])
+    assert np.array_equal(got, flat)
+
+
 @pytest.mark.parametrize("R", [1, 2, 4, 7, 8, 16, 56])
 def test_dispatch_counts(mr, R):
     cfg = gen.cfg3(3000)
