@@ -1,8 +1,9 @@
 // route_decode.cu -- decode-size routing (T <= 64) in one launch of one thread-block
 // cluster, plus the sigmoid table and elementwise score kernels.
 //
-// Decode rows are few (8-64 per step), so the kernel is latency-bound: one CTA of 8
-// warps per 8 rows, up to 8 CTAs in one cluster.  Each warp routes one row (the
+// Decode rows are few (8-64 per step), so the kernel is latency-bound: CTAs of 8 warps
+// holding up to 8 rows each (one CTA up to 5 rows, then 2..4 rows per CTA over up to 16
+// CTAs; see decode_ctas), all in one cluster.  Each warp routes one row (the
 // prior art on the pages, FlashInfer's routingIndicesClusterKernel for
 // Tier<896, 16>, also ran decode routing as one cluster -- sglang PR #37).  The
 // histogram, scan and stable permutation need every row's ids.  After routing, each
@@ -25,6 +26,7 @@ namespace moe {
 constexpr int kDecodeRowsPerCta = 8;
 constexpr int kDecodeThreads = 32 * kDecodeRowsPerCta;
 constexpr int kDecodeMaxCtas = 16;  // clusters of 16 where the GPU schedules them, else 8
+constexpr int kDecodeMaxRows = 64;  // row masks are 64 bits
 int g_decode_max_ctas = 8;
 
 __host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -50,7 +52,6 @@ static_assert(DecodeSmem<DT_F32>::total <= 227 * 1024, "decode smem (f32) exceed
 static_assert(DecodeSmem<DT_BF16>::total <= 227 * 1024, "decode smem (bf16) exceeds 227 KB");
 static_assert(DecodeSmem<DT_SCORE>::total <= 227 * 1024, "decode smem (scores) exceeds 227 KB");
 static_assert(DecodeSmem<DT_PACKED>::total <= 227 * 1024, "decode smem (index) exceeds 227 KB");
-// row masks are 64 bits: the launcher takes at most 64 rows
 
 // Exclusive scan over the bins of counts popc(mask[e]) into offs[0..n], offs[n] = total,
 // by the whole block: thread i takes the bins [i per, i per + per), per = ceil(n / 256)
@@ -348,7 +349,7 @@ static cudaError_t launch_decode_t(cudaLaunchConfig_t& cfg, const RouteArgs& a) 
 }
 
 cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) {
-  if (a.T > kDecodeRowsPerCta * kDecodeMaxCtas) return cudaErrorInvalidValue;
+  if (a.T > kDecodeMaxRows) return cudaErrorInvalidValue;
   const int ctas = decode_ctas(a.T);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, 1, 1);
