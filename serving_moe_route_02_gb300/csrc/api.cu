@@ -366,6 +366,9 @@ int moe_route_decode_ctas(int T) {
 
 int moe_route_empty(int ctas, struct CUstream_st* stream) {
   if (ctas < 1 || ctas > 16) return MOE_ROUTE_E_INVALID_ARG;
+  DevState* d = nullptr;  // the kernel attributes (clusters above 8) are set with the state
+  const int rc = get_state(reinterpret_cast<cudaStream_t>(stream), &d);
+  if (rc != MOE_ROUTE_OK) return rc;
   return launch_empty(ctas, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? MOE_ROUTE_OK
                                                                                      : MOE_ROUTE_E_CUDA;
 }
