@@ -173,5 +173,45 @@ def cfg_bf16_patterns(T: int, E: int = E_KIMI, off: int = 0, cnt: int = 0, seed:
                 G=G_KIMI, Kg=KG_KIMI, scale=SCALE_KIMI, off=off, cnt=cnt)
 
 
+def cfg_decision_edges(kind: str, T: int = 3000, E: int = E_KIMI, off: int = 0, cnt: int = 0) -> dict:
+    """bf16 inputs that put every decision of the routing on its hardest path:
+      flat        all logits 0 and bias 0: every score, group score and top-k value ties;
+      group_copy  prefill logits with group 5 a copy of group 2 (logits and bias), so two
+                  group scores are equal in every row;
+      group_near  as group_copy, but group 5's biases are one float step above group 2's,
+                  so the two group scores differ by a few float steps;
+      negative    prefill logits, bias ~U(-2.1, -1.9): every biased score is negative;
+      large_bias  prefill logits, bias ~U(-50, 50);
+      plateau     N(0,1) logits (seed 10) with 200 seeded experts per row (seed 11) at 4.0 and
+                  bias 0, so the k-th largest score is shared by far more than k experts.
+    """
+    G = G_KIMI
+    gsz = E // G
+    base = cfg3(T, E, off, cnt)
+    logits = base["logits"].copy()
+    bias = base["bias"].copy()
+    if kind == "flat":
+        logits[:] = 0
+        bias[:] = 0.0
+    elif kind in ("group_copy", "group_near"):
+        logits[:, 5 * gsz:6 * gsz] = logits[:, 2 * gsz:3 * gsz]
+        bias[5 * gsz:6 * gsz] = bias[2 * gsz:3 * gsz]
+        if kind == "group_near":
+            bias[5 * gsz:6 * gsz] = np.nextafter(bias[5 * gsz:6 * gsz], np.float32(np.inf))
+    elif kind == "negative":
+        bias = uniform_f32(1, E, -2.1, -1.9)
+    elif kind == "large_bias":
+        bias = uniform_f32(1, E, -50.0, 50.0)
+    elif kind == "plateau":
+        x = normal_f32(10, T * E).reshape(T, E)
+        cols = (raw64(11, T * 200) % np.uint64(E)).astype(np.int64).reshape(T, 200)
+        x[np.arange(T)[:, None], cols] = 4.0
+        logits = f32_to_bf16_bits(x)
+        bias[:] = 0.0
+    else:
+        raise ValueError(kind)
+    return dict(base, logits=logits, bias=bias)
+
+
 def num_local_experts(E: int, ep: int) -> int:
     return E // ep

@@ -205,10 +205,11 @@ int moe_route_padded_capacity(int T, int k, int NE, int tile);
 int moe_route_bins(int E, int k, int local_count);
 
 /*
- * Policy helper (sglang PR #37: rank-local ids apply only to "a proper sub-range that
- * shrinks the routing problem"): returns round_up(local_count + k, 4) when
- * 0 < local_count < E and that is smaller than E; otherwise E, meaning the caller
- * should pass local_count = 0 (global ids).
+ * Policy helper.  The page applies rank-local ids only when the rank's expert range is
+ * strictly smaller than the whole set and relabelling makes the routing problem smaller
+ * (sglang PR #37, Rank-local expert ids for the EP routed MoE, description).  Returns
+ * round_up(local_count + k, 4) when 0 < local_count < E and that is smaller than E;
+ * otherwise E, meaning the caller should pass local_count = 0 (global ids).
  */
 int moe_route_num_experts(int E, int k, int local_offset, int local_count);
 
@@ -233,10 +234,27 @@ int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream
 /*
  * Kernel selection for moe_route: 0 = automatic (T <= 64: one-cluster decode kernel,
  * otherwise the persistent multi-CTA kernel), 1 = always the decode kernel (T <= 64
- * only), 2 = always the persistent kernel.  Process-wide; for tests and benchmarks.
+ * only), 2 = always the persistent kernel, 3 = always the persistent kernel and, for
+ * bf16 logits with k = 16 and topk_group = 4, its variant that computes every score
+ * from the exact table instead of the one that starts from approximate scores (the
+ * results are identical; for comparisons).  Process-wide; for tests and benchmarks.
  * Returns the previous setting, or MOE_ROUTE_E_INVALID_ARG.
  */
 int moe_route_set_path(int path);
+
+/*
+ * Test hook for the failure path of the persistent kernel's grid barrier.  The pages
+ * describe no counterpart.  Arms the next moe_route call on this process that launches
+ * the persistent kernel: its CTA `cta` leaves before the first grid barrier without
+ * arriving, and every grid-barrier wait of that launch is limited to wait_us
+ * microseconds, so the other CTAs' waits run out, set MOE_ROUTE_E_DEVICE_TIMEOUT
+ * (moe_route_device_status) and return; the last CTA out restores the barrier words,
+ * so the following call runs normally.  Nothing waits without a bound.  The arming is
+ * consumed by that one launch.  cta = -1 disarms.  INVALID_ARG for cta < -1, or
+ * wait_us outside [1, 2000000] when cta >= 0.  A cta at or beyond the launch's CTA
+ * count arms nothing that happens.
+ */
+int moe_route_arm_barrier_timeout(int cta, int wait_us);
 
 /*
  * moe_route_noalloc -- moe_route for callers that cannot allocate device memory.
@@ -249,8 +267,10 @@ int moe_route_set_path(int path);
  * given, uses this entry point instead: it never calls cudaMalloc, cudaFree or any
  * allocating routine.  Its scratch is a fixed array in the library's device image,
  * about 1.4 MB, held by every GPU that loads the library until the process exits.
- *   - Arguments, outputs and results are those of moe_route.  It always runs the
- *     persistent multi-CTA kernel (T = 0 writes zero counts and offsets only).
+ *   - Arguments, outputs and results are those of moe_route.  It runs the persistent
+ *     multi-CTA kernel for every T >= 1 (for bf16 logits with k = 16 and topk_group = 4
+ *     the variant moe_route uses for such batches); T = 0 launches the decode kernel,
+ *     which writes zero counts and offsets only.
  *   - status: nullable DEVICE pointer to one int32 the call sets to 0, then to
  *     MOE_ROUTE_E_DEVICE_TIMEOUT if a bounded device-side wait runs out.  With NULL,
  *     such an error is recorded only inside the library's array.

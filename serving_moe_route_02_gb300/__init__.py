@@ -68,6 +68,8 @@ def load(path: str | None = None):
     lib.moe_route_sigmoid.restype = I
     lib.moe_route_set_path.argtypes = [I]
     lib.moe_route_set_path.restype = I
+    lib.moe_route_arm_barrier_timeout.argtypes = [I, I]
+    lib.moe_route_arm_barrier_timeout.restype = I
     lib.moe_route_noalloc.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
     lib.moe_route_noalloc.restype = I
     lib.moe_route_layout.argtypes = [P, P, P, I, I, I, I, P, P, P, P, I, P]

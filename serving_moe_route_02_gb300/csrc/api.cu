@@ -2,6 +2,7 @@
 // dispatch to the routing kernels.  No routing arithmetic happens on the host.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -14,9 +15,11 @@ namespace {
 using namespace moe;
 
 struct DevState {
-  bool ready = false;
+  std::atomic<bool> ready{false};  // set (release) once everything below is in place
   int nsm = 0;
   int blocks_per_sm = 0;
+  int fast_blocks_per_sm = 0;  // the approximate-score persistent kernel
+  float eps_half = 0.0f;       // its measured approximation bound (route_fast.cuh)
   float* stab = nullptr;  // sigmoid table for bf16 logits
   float2* etab = nullptr; // 2^(j/64) table for float32 logits
   int* err = nullptr;     // device status word
@@ -29,6 +32,10 @@ constexpr int kMaxDevices = 64;
 DevState g_dev[kMaxDevices];
 std::mutex g_mu;
 int g_path = 0;
+// moe_route_arm_barrier_timeout: the next persistent launch's skipped CTA (-1: none) and
+// grid-barrier wait limit
+std::atomic<int> g_skip_cta{-1};
+std::atomic<unsigned long long> g_skip_wait_ns{0};
 
 bool capturing(cudaStream_t st) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -45,6 +52,7 @@ int init_device(DevState& d) {
   if (setup_decode_kernels() != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (setup_prefill_kernels(&d.blocks_per_sm) != cudaSuccess || d.blocks_per_sm < 1)
     return MOE_ROUTE_E_CUDA;
+  if (setup_prefill_fast(&d.fast_blocks_per_sm) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   const int grid_max = d.nsm * d.blocks_per_sm;
   const size_t n_tab = size_t(kSigTablePad);
   const size_t n_hist = size_t(kMaxBins) * grid_max;
@@ -71,8 +79,16 @@ int init_device(DevState& d) {
   d.gscores = reinterpret_cast<float*>(d.pw.bar + 16);
   d.pw.grid_max = grid_max;
   if (launch_sigmoid_table(d.stab, d.etab, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  // the approximation bound of the fast persistent kernel, measured into a spare word of
+  // the zeroed workspace and read back (the word is zeroed again afterwards)
+  unsigned* probe = d.pw.bar + 4;
+  if (launch_approx_err(probe, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
-  d.ready = true;
+  unsigned bits = 0;
+  if (cudaMemcpy(&bits, probe, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (cudaMemset(probe, 0, sizeof(bits)) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  std::memcpy(&d.eps_half, &bits, sizeof(bits));
+  d.ready.store(true, std::memory_order_release);
   return MOE_ROUTE_OK;
 }
 
@@ -81,10 +97,10 @@ int get_state(cudaStream_t st, DevState** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ROUTE_E_CUDA;
   DevState& d = g_dev[dev];
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     if (st != nullptr && capturing(st)) return MOE_ROUTE_E_WORKSPACE;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       const int rc = init_device(d);
       if (rc != MOE_ROUTE_OK) return rc;
     }
@@ -166,6 +182,7 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
   a.cnt = local_count;
   a.NE = bins(E, k, local_count);
   a.scale = scale;
+  a.eps_half = d->eps_half;
   const int dt = logits_dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32;
 
   const bool decode = (g_path == 1) || (g_path == 0 && T <= 64);
@@ -177,11 +194,26 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
     if (T == 0) {
       ce = launch_route_decode(a, dt, st);
     } else {
-      const int grid_cap = d->pw.grid_max;
-      int grid = (T + 15) / 16;
-      if (grid > grid_cap) grid = grid_cap;
-      if (!prefill_fits(T, grid)) return MOE_ROUTE_E_UNSUPPORTED;
-      ce = launch_route_prefill(a, dt, d->pw, grid, st);
+      const int skip = g_skip_cta.exchange(-1);
+      if (skip >= 0) {
+        a.barrier_skip_cta = skip;
+        a.barrier_wait_ns = g_skip_wait_ns.load();
+      }
+      // bf16 logits of the Kimi-K3 instance: the persistent kernel on approximate scores
+      // (path 3 forces the exact-score kernel, for comparisons)
+      int grid_fast = d->nsm * d->fast_blocks_per_sm;
+      if (grid_fast > d->pw.grid_max) grid_fast = d->pw.grid_max;
+      if (grid_fast > (T + 15) / 16) grid_fast = (T + 15) / 16;
+      if (dt == DT_BF16 && k == 16 && topk_group == 4 && g_path != 3 && grid_fast >= 1 &&
+          prefill_fast_fits(T, grid_fast)) {
+        ce = launch_route_prefill_fast(a, d->pw, grid_fast, st);
+      } else {
+        const int grid_cap = d->pw.grid_max;
+        int grid = (T + 15) / 16;
+        if (grid > grid_cap) grid = grid_cap;
+        if (!prefill_fits(T, grid)) return MOE_ROUTE_E_UNSUPPORTED;
+        ce = launch_route_prefill(a, dt, d->pw, grid, st);
+      }
     }
   }
   return ce == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
@@ -350,10 +382,17 @@ int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream
 }
 
 int moe_route_set_path(int path) {
-  if (path < 0 || path > 2) return MOE_ROUTE_E_INVALID_ARG;
+  if (path < 0 || path > 3) return MOE_ROUTE_E_INVALID_ARG;
   const int prev = g_path;
   g_path = path;
   return prev;
+}
+
+int moe_route_arm_barrier_timeout(int cta, int wait_us) {
+  if (cta < -1 || (cta >= 0 && (wait_us < 1 || wait_us > 2000000))) return MOE_ROUTE_E_INVALID_ARG;
+  g_skip_wait_ns.store(static_cast<unsigned long long>(cta >= 0 ? wait_us : 0) * 1000ull);
+  g_skip_cta.store(cta);
+  return MOE_ROUTE_OK;
 }
 
 int moe_route_decode_ctas(int T) {

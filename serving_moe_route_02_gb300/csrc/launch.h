@@ -48,9 +48,17 @@ cudaError_t launch_router_gemm(const uint16_t* hidden, const uint16_t* w, float*
                                float* scores, const float2* etab, int T, int H, int E, int* err,
                                cudaStream_t st);
 cudaError_t setup_prefill_kernels(int* blocks_per_sm);
-// False when a warp of the persistent kernel would get 65,536 rows or more (its 16-bit
-// bin counters would overflow); the launcher then refuses the launch.
+// True when the persistent kernel can take T rows on `grid` CTAs (T >= 0, grid >= 1).
 bool prefill_fits(int T, int grid);
+// The persistent kernel for bf16 logits with k = 16 and topk_group = 4, built on
+// approximate scores (route_prefill_fast.cu).  prefill_fast_fits: T rows on `grid` CTAs
+// fit its per-warp entry room.
+cudaError_t setup_prefill_fast(int* blocks_per_sm);
+bool prefill_fast_fits(int T, int grid);
+cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, int grid,
+                                      cudaStream_t st);
+// Writes the bits of E_half (route_fast.cuh) to *out, which must hold 0.
+cudaError_t launch_approx_err(unsigned* out, cudaStream_t st);
 // The argument checks of moe_route (status code; MOE_ROUTE_OK when the call is valid).
 int route_args_status(int T, int E, int k, int n_group, int topk_group, int off, int cnt);
 cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,

@@ -11,7 +11,9 @@
 // (about 1.4 MB) until the process exits.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/moe_route.h"
@@ -33,16 +35,19 @@ constexpr size_t o_prefix = o_hist + kHistBytes;
 constexpr size_t o_counts = o_prefix + kHistBytes;
 constexpr size_t o_bar = o_counts + size_t(kMaxBins) * 4;   // 2 words
 constexpr size_t o_err = o_bar + 8;                          // 1 word
-constexpr size_t kNoallocBytes = (o_err + 4 + 255) / 256 * 256;
+constexpr size_t o_probe = o_err + 4;                        // 1 word (set-up only)
+constexpr size_t kNoallocBytes = (o_probe + 4 + 255) / 256 * 256;
 
 // The scratch.  In host code this name is only a stand-in for the device object; the
 // device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
 struct NoallocDev {
-  bool ready = false;
-  unsigned char* base = nullptr;  // device address of g_noalloc_scratch on this device
+  std::atomic<bool> ready{false};  // set (release) once the fields below are in place
+  unsigned char* base = nullptr;   // device address of g_noalloc_scratch on this device
   int grid_max = 0;
+  int grid_fast = 0;               // CTAs of the approximate-score persistent kernel
+  float eps_half = 0.0f;           // its measured approximation bound
 };
 NoallocDev g_na[64];
 std::mutex g_na_mu;
@@ -53,20 +58,28 @@ int noalloc_setup(int dev, NoallocDev& d) {
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
     return MOE_ROUTE_E_CUDA;
-  int nsm = 0, bpsm = 0;
+  int nsm = 0, bpsm = 0, fbpsm = 0;
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return MOE_ROUTE_E_CUDA;
   if (setup_decode_kernels() != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (setup_prefill_kernels(&bpsm) != cudaSuccess || bpsm < 1) return MOE_ROUTE_E_CUDA;
+  if (setup_prefill_fast(&fbpsm) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   unsigned char* base = static_cast<unsigned char*>(p);
   if (launch_sigmoid_table(reinterpret_cast<float*>(base + o_tab),
                            reinterpret_cast<float2*>(base + o_exp), nullptr) != cudaSuccess)
     return MOE_ROUTE_E_CUDA;
-  if (cudaMemset(base + o_bar, 0, 12) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (cudaMemset(base + o_bar, 0, o_probe + 4 - o_bar) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (launch_approx_err(reinterpret_cast<unsigned*>(base + o_probe), nullptr) != cudaSuccess)
+    return MOE_ROUTE_E_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpy(&bits, base + o_probe, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ROUTE_E_CUDA;
+  std::memcpy(&d.eps_half, &bits, sizeof(bits));
   d.base = base;
   d.grid_max = nsm * bpsm < kNoallocMaxCtas ? nsm * bpsm : kNoallocMaxCtas;
-  d.ready = true;
+  d.grid_fast = nsm * fbpsm < kNoallocMaxCtas ? nsm * fbpsm : kNoallocMaxCtas;
+  d.ready.store(true, std::memory_order_release);
   return MOE_ROUTE_OK;
 }
 
@@ -101,13 +114,13 @@ extern "C" int moe_route_noalloc(const void* logits, int logits_dtype, const flo
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ROUTE_E_CUDA;
   NoallocDev& d = g_na[dev];
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (!d.ready) {
+  if (!d.ready.load(std::memory_order_acquire)) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (st != nullptr && cudaStreamIsCapturing(st, &cs) == cudaSuccess &&
         cs != cudaStreamCaptureStatusNone)
       return MOE_ROUTE_E_WORKSPACE;  // the first call on a device must not be captured
     std::lock_guard<std::mutex> lk(g_na_mu);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
       const int rc = noalloc_setup(dev, d);
       if (rc != MOE_ROUTE_OK) return rc;
     }
@@ -131,6 +144,7 @@ extern "C" int moe_route_noalloc(const void* logits, int logits_dtype, const flo
   a.cnt = local_count;
   a.NE = NE;
   a.scale = scale;
+  a.eps_half = d.eps_half;
   const int dt = logits_dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32;
 
   // words that must start at zero: the caller's status word and the grid barrier
@@ -144,6 +158,10 @@ extern "C" int moe_route_noalloc(const void* logits, int logits_dtype, const flo
   ws.counts = reinterpret_cast<int*>(d.base + o_counts);
   ws.bar = reinterpret_cast<unsigned*>(d.base + o_bar);
   ws.grid_max = kNoallocMaxCtas;
+  // the same kernel choice as moe_route for T > 64 rows
+  int grid_fast = d.grid_fast < (T + 15) / 16 ? d.grid_fast : (T + 15) / 16;
+  if (dt == DT_BF16 && k == 16 && topk_group == 4 && grid_fast >= 1 && prefill_fast_fits(T, grid_fast))
+    return launch_route_prefill_fast(a, ws, grid_fast, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
   int grid = (T + 15) / 16;
   if (grid > d.grid_max) grid = d.grid_max;
   if (!prefill_fits(T, grid)) return MOE_ROUTE_E_UNSUPPORTED;

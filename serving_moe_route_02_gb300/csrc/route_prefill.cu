@@ -22,7 +22,7 @@
 // the device status word and the kernel returns.
 #include <cooperative_groups.h>
 
-#include "launch.h"
+#include "persist.cuh"
 
 namespace moe {
 
@@ -89,78 +89,6 @@ __device__ __forceinline__ bool repeated_in_row(int l, unsigned kmask, int k) {
   return n > 1;
 }
 
-// Grid-wide barrier for a cooperative launch, bounded in time.  One arrival counter:
-// CTA 0 adds 2^31 - (nblocks - 1), every other CTA adds 1, so the counter's top bit
-// flips exactly when all have arrived (it starts at 0 and every completed barrier
-// leaves it at 0 or 2^31).  Returns false if the wait ran out.
-__device__ bool grid_barrier(unsigned* bar, unsigned nblocks, int* err, int* flag_s) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned add = (blockIdx.x == 0) ? 0x80000000u - (nblocks - 1u) : 1u;
-    unsigned old;
-    // release: the CTA's writes ordered before it by the block barrier above
-    asm volatile("atom.release.gpu.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(bar), "r"(add) : "memory");
-    int ok = 1;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-      unsigned cur;
-      asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(cur) : "l"(bar) : "memory");
-      if ((cur ^ old) & 0x80000000u) break;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        atomicExch(err, kErrTimeout);
-        ok = 0;
-        break;
-      }
-    }
-    *flag_s = ok;
-  }
-  __syncthreads();
-  return *flag_s != 0;
-}
-
-// Exclusive scan of in[0..n) into out[0..n], out[n] = total, with two block barriers.
-// All threads of the block call it; `tmp` holds at least 32 ints.  in and out may alias.
-__device__ __forceinline__ void block_scan_fast(const int* in, int* out, int n, int* tmp) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int lane = tid & 31, wid = tid >> 5;
-  const int per = (n + nt - 1) / nt;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-  int v[4];
-  int sum = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[i] = (lo + i < hi) ? in[lo + i] : 0;
-    sum += v[i];
-  }
-  for (int i = lo + 4; i < hi; ++i) sum += in[i];  // only when n > 4 * blockDim.x
-  int incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) tmp[wid] = incl;
-  __syncthreads();
-  int run = incl - sum;
-  for (int i = 0; i < wid; ++i) run += tmp[i];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (lo + i < hi) {
-      out[lo + i] = run;
-      run += v[i];
-    }
-  }
-  for (int i = lo + 4; i < hi; ++i) {
-    const int u = in[i];
-    out[i] = run;
-    run += u;
-  }
-  if (hi == n && lo < hi) out[n] = run;
-  if (n == 0 && tid == 0) out[0] = 0;
-  __syncthreads();
-}
-
-// SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).
 // SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).
 template <int DT, bool SPEC>
 __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
@@ -293,43 +221,18 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
   block_scan_fast(hist_s, lbase_s, a.NE, tmp);
 
   int* flag_s = tmp + 32;
-  if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
-
-  // ---- column scan over CTAs, one warp per bin; lane l covers up to 8 consecutive CTAs
-  //      per pass of 256
-  for (int e = cta * NW + w; e < a.NE; e += grid * NW) {
-    const int* h = pw.hist + size_t(e) * pw.grid_max;
-    int* p = pw.prefix + size_t(e) * pw.grid_max;
-    int carry = 0;
-    for (int c0 = 0; c0 < grid; c0 += 256) {
-      const int span = min(256, grid - c0);
-      const int per = (span + 31) / 32;
-      const int cl = c0 + lane * per;
-      int v[8];
-      int sum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        v[i] = (i < per && cl + i < c0 + span) ? __ldcg(h + cl + i) : 0;
-        sum += v[i];
-      }
-      int incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
-      }
-      int run = carry + incl - sum;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (i < per && cl + i < c0 + span) p[cl + i] = run;
-        run += v[i];
-      }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) pw.counts[e] = carry;
+  if (!grid_barrier(pw.bar, grid, a.err, flag_s, a.barrier_wait_ns, a.barrier_skip_cta)) {
+    grid_exit(pw.bar, grid);
+    return;
   }
 
-  if (!grid_barrier(pw.bar, grid, a.err, flag_s)) return;
+  // ---- column scan over CTAs (prefixes and bin totals)
+  column_scan(pw, a.NE, grid, NW);
+
+  if (!grid_barrier(pw.bar, grid, a.err, flag_s, a.barrier_wait_ns)) {
+    grid_exit(pw.bar, grid);
+    return;
+  }
 
   // ---- phase 3: offsets, then this CTA's permutation entries (bin totals and this CTA's
   //      prefixes are loaded together: one round trip)
@@ -459,6 +362,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
     __syncthreads();
     for (int i = tid; i < nvalid; i += NT) a.perm[base_s[sbin[i]] + i] = sval[i];
   }
+  grid_exit(pw.bar, grid);
 }
 
 template <int DT, bool SPEC>

@@ -35,6 +35,12 @@ struct RouteArgs {
   int* err;               // device status word
   int T, k, Kg, off, cnt, NE;
   float scale;
+  float eps_half;         // bound on |0.5 tanh.approx(x / 2) - (sigmoid(x) - 0.5)| over
+                          // bf16 x, measured on the device (route_fast.cuh)
+  uint64_t barrier_wait_ns = kWaitLimitNs;  // limit of each grid-barrier wait of the
+                                            // persistent kernels
+  int barrier_skip_cta = -1;  // CTA that leaves before the first grid barrier (-1: none;
+                              // a test of the timeout path)
 };
 
 // Per-warp shared scratch of the row routine.  NB = biased scores parked by the kept

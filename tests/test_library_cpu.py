@@ -50,6 +50,12 @@ def test_host_helpers(libpath):
     assert lib.moe_route_set_path(5) == mr.E_INVALID_ARG
     prev = mr.set_path(2)
     assert mr.set_path(prev) == 2
+    assert lib.moe_route_set_path(3) >= 0 and mr.set_path(prev) == 3
+    # the barrier test hook validates its arguments on the host (and is left disarmed)
+    assert lib.moe_route_arm_barrier_timeout(-2, 0) == mr.E_INVALID_ARG
+    assert lib.moe_route_arm_barrier_timeout(0, 0) == mr.E_INVALID_ARG
+    assert lib.moe_route_arm_barrier_timeout(0, 2000001) == mr.E_INVALID_ARG
+    assert lib.moe_route_arm_barrier_timeout(-1, 0) == mr.OK
 
 
 def test_missing_library_fails_loudly(tmp_path):
