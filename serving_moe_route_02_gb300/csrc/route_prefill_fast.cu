@@ -1,15 +1,17 @@
 // route_prefill_fast.cu -- prefill-size routing of bf16 logits for the Kimi-K3 instance
 // (E = 896 in 8 groups, k = 16, keep 4 groups) in one persistent, cooperative launch:
-// one CTA of 16 warps per SM, a contiguous row range per CTA and per warp.
+// one CTA of 16 warps per SM, a contiguous row range per CTA and per warp.  The exact
+// score table stays in global memory (read through the L1 cache): only the survivors of
+// each row, about 18 of 896, and the rare exact group scores look it up.
 //
-// Phase 1 (streaming): every warp keeps D rows in flight with one-dimensional bulk
-//   copies into a private ring in shared memory and routes each row with route_row_fast
-//   (approximate scores, exact table lookups only where a decision needs them).  Lanes
-//   0..15 store the packed slots, then count their relabelled ids into the warp's own
-//   16-bit counters (two per 32-bit word); the counter's old value is the entry's rank
-//   among this warp's entries of the same id, in (token, slot) order, since a warp
-//   routes its rows in order and ids are unique in a row.  (id, rank) is kept in shared
-//   memory.
+// Phase 1 (streaming): every warp keeps D pairs of rows in flight with one-dimensional
+//   bulk copies into a private ring in shared memory and routes each pair with route_pair
+//   (lanes 0-15 the first row, 16-31 the second; approximate scores, exact table lookups
+//   only where a decision needs them).  Lane h of each half stores slot h, then counts
+//   its relabelled id into the warp's own 16-bit counters (two per 32-bit word), first
+//   row first; the counter's old value is the entry's rank among this warp's entries of
+//   the same id, in (token, slot) order, since a warp routes its rows in order and ids
+//   are unique in a row.  (id, rank) is kept in shared memory.
 // CTA tail of phase 1: a column pass over the warps' counters gives each warp's prefix
 //   per id and the CTA's histogram, which goes to the expert-major matrix hist[bin][cta];
 //   a block scan gives the CTA-local bin offsets, and every entry is placed at its
@@ -23,7 +25,7 @@
 #include <cooperative_groups.h>
 
 #include "persist.cuh"
-#include "route_fast.cuh"
+#include "route_pair.cuh"
 
 namespace moe {
 
@@ -33,26 +35,27 @@ __host__ __device__ constexpr int f_align(int x, int a) { return (x + a - 1) / a
 
 struct FastSmem {
   static constexpr int NW = 16;                    // warps per CTA
-  static constexpr int D = 3;                      // rows in flight per warp
+  static constexpr int D = 2;                      // pairs of rows in flight per warp
   static constexpr int ROWB = kE * 2;              // one bf16 row: 1,792 bytes
+  static constexpr int SLOTB = 2 * ROWB;           // a pair of rows
   static constexpr int WORDS = kMaxBins / 2;       // 16-bit counters, two per word
-  static constexpr int o_stab = 0;
-  static constexpr int o_bias = f_align(kSigTablePad * 4, 128);
-  static constexpr int o_ring = f_align(o_bias + kE * 4, 128);
-  static constexpr int o_wcnt = o_ring + NW * D * ROWB;
+  static constexpr int o_bias = 0;
+  static constexpr int o_cpp = f_align(o_bias + kE * 4, 128);   // c'' = bias + 0.5 - o
+  static constexpr int o_ring = f_align(o_cpp + kE * 4, 128);
+  static constexpr int o_wcnt = o_ring + NW * D * SLOTB;
   static constexpr int o_ws = f_align(o_wcnt + NW * WORDS * 4, 128);
-  static constexpr int o_hist = f_align(o_ws + NW * int(sizeof(FastScratch)), 128);
+  static constexpr int o_hist = f_align(o_ws + NW * int(sizeof(PairScratch)), 128);
   static constexpr int o_lbase = f_align(o_hist + (kMaxBins + 1) * 4, 128);
   static constexpr int o_gbase = f_align(o_lbase + (kMaxBins + 1) * 4, 128);
   static constexpr int o_tmp = f_align(o_gbase + (kMaxBins + 1) * 4, 128);
   static constexpr int o_mbar = f_align(o_tmp + 64 * 4, 128);
   static constexpr int o_ent = f_align(o_mbar + (NW * D + 1) * 8, 128);
   // (id, rank) of each entry, per warp, in the room left
-  static constexpr int ENT_PER_WARP = (227 * 1024 - o_ent) / (NW * 4) / 16 * 16;
+  static constexpr int ENT_PER_WARP = (227 * 1024 - o_ent) / (NW * 4) / 32 * 32;
   static constexpr int ROWS_PER_WARP = ENT_PER_WARP / 16;
   static constexpr int total = o_ent + NW * ENT_PER_WARP * 4;
   // the CTA's sorted entries, in the ring once phase 1 is over: values, then bins
-  static constexpr int SORT_CAP = (NW * D * ROWB) / 6 / 8 * 8;
+  static constexpr int SORT_CAP = (NW * D * SLOTB) / 6 / 8 * 8;
   static constexpr int o_sval = o_ring;
   static constexpr int o_sbin = o_ring + SORT_CAP * 4;
 };
@@ -74,11 +77,11 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   constexpr int NT = NW * 32;
   constexpr int K = 16;
   extern __shared__ __align__(128) uint8_t smem[];
-  float* stab = reinterpret_cast<float*>(smem + L::o_stab);
   float* bias_s = reinterpret_cast<float*>(smem + L::o_bias);
+  float* cpp_s = reinterpret_cast<float*>(smem + L::o_cpp);
   uint8_t* ring_all = smem + L::o_ring;
   uint32_t* wcnt_all = reinterpret_cast<uint32_t*>(smem + L::o_wcnt);
-  FastScratch* wsp = reinterpret_cast<FastScratch*>(smem + L::o_ws);
+  PairScratch* wsp = reinterpret_cast<PairScratch*>(smem + L::o_ws);
   int* hist_s = reinterpret_cast<int*>(smem + L::o_hist);
   int* lbase_s = reinterpret_cast<int*>(smem + L::o_lbase);
   int* gbase_s = reinterpret_cast<int*>(smem + L::o_gbase);
@@ -95,7 +98,8 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   const int wr0 = min(r1, r0 + w * per_warp);
   const int wr1 = min(r1, wr0 + per_warp);
   const int nw = wr1 - wr0;  // <= ROWS_PER_WARP (checked by the launcher)
-  uint8_t* ring = ring_all + w * L::D * L::ROWB;
+  const int npairs = (nw + 1) / 2;
+  uint8_t* ring = ring_all + w * L::D * L::SLOTB;
   uint64_t* mb = mbar_all + w * L::D;
   uint32_t* wcnt = wcnt_all + w * L::WORDS;
   uint32_t* ent = reinterpret_cast<uint32_t*>(smem + L::o_ent) + w * L::ENT_PER_WARP;
@@ -112,77 +116,91 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   for (int i = tid; i < NW * L::WORDS; i += NT) wcnt_all[i] = 0u;
   __syncthreads();
   if (tid == 0) {
-    mbar_expect_tx(tab_bar, uint32_t(kSigTablePad * 4 + kE * 4));
-    bulk_g2s(stab, a.stab, kSigTablePad * 4, tab_bar);
+    mbar_expect_tx(tab_bar, uint32_t(kE * 4));
     bulk_g2s(bias_s, a.bias, kE * 4, tab_bar);
   }
+  // rows 2p and 2p + 1 of this warp (the second may not exist) into slot p % D
+  auto issue_pair = [&](int p) {
+    const int slot = p % L::D;
+    const uint32_t bytes = uint32_t(min(2, nw - 2 * p)) * L::ROWB;
+    mbar_expect_tx(mb + slot, bytes);
+    bulk_g2s(ring + slot * L::SLOTB, logits + size_t(wr0 + 2 * p) * L::ROWB, bytes, mb + slot);
+  };
   if (lane == 0) {
-    for (int d = 0; d < L::D && d < nw; ++d) {
-      mbar_expect_tx(mb + d, L::ROWB);
-      bulk_g2s(ring + d * L::ROWB, logits + size_t(wr0 + d) * L::ROWB, L::ROWB, mb + d);
-    }
+    for (int d = 0; d < L::D && d < npairs; ++d) issue_pair(d);
   }
   // first row whose wait ran out (-1: none); 0 also when the table never arrived
   int fail_at = mbar_wait_bounded(tab_bar, 0, a.err) ? -1 : 0;
 
-  // error bounds of the approximate scores: B = max |bias| over the experts
-  float bmax;
+  // error bounds of the approximate scores: the biases' range
+  PairBounds pbnd;
   {
-    float m = 0.0f;
-    for (int e = tid; e < kE; e += NT) m = fmaxf(m, fabsf(bias_s[e]));
-    const uint32_t wm = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-    if (lane == 0) tmp[w] = int(wm);
-    __syncthreads();
-    uint32_t bm = 0;
-#pragma unroll
-    for (int i = 0; i < NW; ++i) bm = max(bm, uint32_t(tmp[i]));
-    bmax = __uint_as_float(bm);
-  }
-  const ApproxBounds bnd = approx_bounds(a.eps_half, bmax);
-  // this lane's 0.5 + bias (registers for the whole launch)
-  float c[kEPL];
-  {
-    const float4* bq = reinterpret_cast<const float4*>(bias_s + lane * kEPL);
-#pragma unroll
-    for (int q = 0; q < kEPL / 4; ++q) {
-      const float4 v = bq[q];
-      c[4 * q + 0] = __fadd_rn(0.5f, v.x);
-      c[4 * q + 1] = __fadd_rn(0.5f, v.y);
-      c[4 * q + 2] = __fadd_rn(0.5f, v.z);
-      c[4 * q + 3] = __fadd_rn(0.5f, v.w);
+    float mx = -INFINITY, mn = INFINITY;
+    for (int e = tid; e < kE; e += NT) {
+      mx = fmaxf(mx, bias_s[e]);
+      mn = fminf(mn, bias_s[e]);
     }
+    // order-preserving keys, so that integer reductions give the float max and min
+    const uint32_t kmx = __reduce_max_sync(0xffffffffu, fkey(mx));
+    const uint32_t kmn = __reduce_min_sync(0xffffffffu, fkey(mn));
+    if (lane == 0) {
+      tmp[w] = int(kmx);
+      tmp[16 + w] = int(kmn);
+    }
+    __syncthreads();
+    uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      bmx = max(bmx, uint32_t(tmp[i]));
+      bmn = min(bmn, uint32_t(tmp[16 + i]));
+    }
+    pbnd = pair_bounds(a.eps_half, fkey_inv(bmn), fkey_inv(bmx));
   }
+  for (int e = tid; e < kE; e += NT) cpp_s[e] = __fadd_rn(bias_s[e], pbnd.d0);
+  __syncthreads();
 
-  // ---- phase 1: route this warp's rows, rank their entries within the warp
-  for (int i = 0; i < nw && fail_at < 0; ++i) {
-    const int slot = i % L::D;
-    const uint32_t par = uint32_t(i / L::D) & 1u;
+  // ---- phase 1: route this warp's rows two at a time, rank their entries within the warp
+  const int half = lane >> 4, h = lane & 15;
+  for (int p = 0; p < npairs && fail_at < 0; ++p) {
+    const int slot = p % L::D;
+    const uint32_t par = uint32_t(p / L::D) & 1u;
     if (!mbar_wait_bounded(mb + slot, par, a.err)) {
-      fail_at = i;
+      fail_at = p;
       break;
     }
+    const uint8_t* r0p = ring + slot * L::SLOTB;
+    const bool has1 = 2 * p + 1 < nw;
+    const SlotOut o = route_pair(r0p, has1 ? r0p + L::ROWB : r0p, bias_s, cpp_s, a.stab, pbnd, a, wsp[w]);
+    const int i = 2 * p + half;  // this half's row within the warp
+    const bool valid = i < nw;
     const int t = wr0 + i;
-    const SlotOut o = route_row_fast(ring + slot * L::ROWB, bias_s, stab, c, bnd, a, wsp[w]);
-    if (lane < K) {
-      a.packed[size_t(t) * K + lane] = o.packed;
-      if (a.ids) a.ids[size_t(t) * K + lane] = o.id;
-      const uint32_t sh = uint32_t(o.lid & 1) * 16u;
+    if (valid) {
+      a.packed[size_t(t) * K + h] = o.packed;
+      if (a.ids) a.ids[size_t(t) * K + h] = o.id;
+    }
+    // ranks: the first row's entries before the second row's
+    const uint32_t sh = uint32_t(o.lid & 1) * 16u;
+    if (half == 0) {
       const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
-      ent[i * K + lane] = uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 16);
+      ent[i * K + h] = uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 16);
     }
     __syncwarp();
-    if (lane == 0 && i + L::D < nw) {
+    if (half == 1 && valid) {
+      const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
+      ent[i * K + h] = uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 16);
+    }
+    __syncwarp();
+    if (lane == 0 && p + L::D < npairs) {
       fence_proxy_async_smem();
-      mbar_expect_tx(mb + slot, L::ROWB);
-      bulk_g2s(ring + slot * L::ROWB, logits + size_t(t + L::D) * L::ROWB, L::ROWB, mb + slot);
+      issue_pair(p + L::D);
     }
   }
-  // after a wait that ran out, the copies issued for rows fail_at .. fail_at + D - 1 may
+  // after a wait that ran out, the copies issued for pairs fail_at .. fail_at + D - 1 may
   // still be owed to the ring: wait for them (bounded) before the ring is reused
   if (fail_at >= 0 && lane == 0) {
     if (w == 0) mbar_wait_bounded(tab_bar, 0, nullptr);
-    for (int r = fail_at; r < nw && r < fail_at + L::D; ++r)
-      mbar_wait_bounded(mb + r % L::D, uint32_t(r / L::D) & 1u, nullptr);
+    for (int q = fail_at; q < npairs && q < fail_at + L::D; ++q)
+      mbar_wait_bounded(mb + q % L::D, uint32_t(q / L::D) & 1u, nullptr);
   }
   __syncthreads();
 
@@ -203,7 +221,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   block_scan_fast(hist_s, lbase_s, a.NE, tmp);
   // every routed entry to its CTA-local sorted position (the ring is free now); after a
   // wait that ran out only the rows before it were routed and counted
-  const int nrouted = fail_at < 0 ? nw : fail_at;
+  const int nrouted = fail_at < 0 ? nw : 2 * fail_at;
   for (int x = lane; x < nrouted * K; x += 32) {
     const uint32_t v = ent[x];
     const int l = int(v & 0xFFFFu);
