@@ -68,6 +68,10 @@ def _bind(lib):
     lib.oracle_dispatch_counts.restype = I
     lib.oracle_alltoall_layout.argtypes = [P, I, I, P, P, P]
     lib.oracle_alltoall_layout.restype = I
+    lib.oracle_mxfp4_quant.argtypes = [P, I, I, P, P]
+    lib.oracle_mxfp4_quant.restype = I
+    lib.oracle_e2m1_encode.argtypes = [ctypes.c_double]
+    lib.oracle_e2m1_encode.restype = ctypes.c_uint8
     return lib
 
 
@@ -189,3 +193,20 @@ def alltoall_layout(matrix: np.ndarray, me: int, lib=None) -> dict:
     if rc != 0:
         raise ValueError("oracle_alltoall_layout rejected its arguments")
     return dict(send_displs=sd, recv_counts=rcnt, recv_displs=rd)
+
+
+def mxfp4_quant(x: np.ndarray, lib=None) -> dict:
+    """MXFP4 codes q [T, H / 2] (two E2M1 codes per byte, even element low) and E8M0
+    scales [T, H / 32] of bf16 activations x [T, H] (see oracle_mxfp4_quant)."""
+    xa = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H = xa.shape
+    q = np.empty((T, H // 2), np.uint8)
+    sc = np.empty((T, H // 32), np.uint8)
+    rc = (lib or load()).oracle_mxfp4_quant(_ptr(xa), T, H, _ptr(q), _ptr(sc))
+    if rc != 0:
+        raise ValueError("oracle_mxfp4_quant rejected its arguments")
+    return dict(q=q, scales=sc)
+
+
+def e2m1_encode(v: float, lib=None) -> int:
+    return int((lib or load()).oracle_e2m1_encode(float(v)))

@@ -15,6 +15,9 @@
  *       sglang PR #37 (rank-local expert ids for the EP routed MoE), description.
  *   router parameter count (896 x 7168 per layer):
  *       HartsyInference PR #798, section Memory per GPU (0.59 B router parameters).
+ *   activation quantisation of the fused route+quant decode launch (MXFP4 MoE):
+ *       sglang PR #37, description; format read from the OCP Microscaling Formats (MX)
+ *       specification v1.0 (MXFP4: E2M1 elements, 32-element blocks, E8M0 scale).
  *
  * Built with -O2 -ffp-contract=off and without fast-math so that every float
  * operation is one IEEE operation in the order written.
@@ -287,6 +290,58 @@ int oracle_alltoall_layout(const int32_t* matrix, int R, int me, int32_t* send_d
     for (int s = 0; s < R; ++s) {
         recv_counts[s] = matrix[(size_t)s * R + me];
         recv_displs[s + 1] = recv_displs[s] + recv_counts[s];
+    }
+    return 0;
+}
+
+/* E2M1 magnitudes by code (code & 7): sign | exponent (2 bits, bias 1) | mantissa (1 bit);
+ * exponent 0 is the subnormal range (0 and 0.5). */
+static const double kE2M1[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+uint8_t oracle_e2m1_encode(double v) {
+    int neg = signbit(v) ? 1 : 0;
+    double a = fabs(v);
+    if (a > 6.0) a = 6.0;  /* saturate to the largest magnitude */
+    /* nearest magnitude; on an exact tie the code with last bit 0 */
+    int best = 0;
+    for (int c = 1; c < 8; ++c) {
+        double dc = fabs(a - kE2M1[c]);
+        double db = fabs(a - kE2M1[best]);
+        if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+    }
+    return (uint8_t)((neg << 3) | best);
+}
+
+int oracle_mxfp4_quant(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* scales) {
+    if (T < 0 || H <= 0 || H % 32 != 0) return -1;
+    const int nb = H / 32;
+    for (int t = 0; t < T; ++t) {
+        for (int b = 0; b < nb; ++b) {
+            const uint16_t* v = x + (size_t)t * H + (size_t)b * 32;
+            /* shared exponent from the block's largest magnitude */
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs((double)f32_from_bf16(v[i]));
+                if (a > amax) amax = a;
+            }
+            int e;
+            if (amax == 0.0) {
+                e = -127;
+            } else {
+                int ex;
+                frexp(amax, &ex);   /* amax = m 2^ex, m in [0.5, 1): floor(log2) = ex - 1 */
+                e = (ex - 1) - 2;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            scales[(size_t)t * nb + b] = (uint8_t)(e + 127);
+            /* elements: V / 2^e to E2M1, two per byte, the even element low */
+            for (int i = 0; i < 32; i += 2) {
+                uint8_t lo = oracle_e2m1_encode(ldexp((double)f32_from_bf16(v[i]), -e));
+                uint8_t hi = oracle_e2m1_encode(ldexp((double)f32_from_bf16(v[i + 1]), -e));
+                q[(size_t)t * (H / 2) + (size_t)b * 16 + i / 2] = (uint8_t)(lo | (hi << 4));
+            }
+        }
     }
     return 0;
 }

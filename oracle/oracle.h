@@ -108,6 +108,27 @@ int oracle_dispatch_counts(const int32_t* ids, int n, int E, int R, int32_t* sen
 int oracle_alltoall_layout(const int32_t* matrix, int R, int me, int32_t* send_displs,
                            int32_t* recv_counts, int32_t* recv_displs);
 
+/* MXFP4 quantisation of the decode batch's activations, the quant half of the fused
+ * route+quant decode launch (sglang PR #37, description: route_quant_fused, decode
+ * batches up to MAX_TOKENS = 64; the routed MoE is an MXFP4 MoE, Mxfp4MoEMethod).  The
+ * pages do not define the activation format; the reading taken is the MXFP4 format of the
+ * OCP Microscaling Formats (MX) specification v1.0:
+ *   - a block is 32 consecutive elements of a row (H % 32 == 0);
+ *   - shared scale X = 2^e with e = floor(log2(max_i |V_i|)) - 2 (2 is the exponent of
+ *     the largest E2M1 normal, 6 = 1.5 * 2^2), e clamped to [-127, 127]; a block of
+ *     zeros takes e = -127; the scale is stored as E8M0, the byte e + 127;
+ *   - each element P_i = V_i / X rounded to E2M1 (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+ *     4-bit code sign | 2-bit exponent | 1-bit mantissa) to the nearest magnitude, ties to
+ *     the code whose last bit is 0, magnitudes above 6 saturated to 6, the sign taken from
+ *     V_i (so -0 and negative values that round to 0 give code 8);
+ *   - storage: q [T, H / 2] bytes, byte i of a row holding element 2i in its low nibble
+ *     and element 2i + 1 in its high nibble; scales [T, H / 32] bytes.
+ * x: [T, H] bf16 bits.  Returns 0, or -1 when H % 32 != 0 or T < 0. */
+int oracle_mxfp4_quant(const uint16_t* x, int T, int H, uint8_t* q, uint8_t* scales);
+
+/* E2M1 code (0..15) of an already scaled value, by the rule above. */
+uint8_t oracle_e2m1_encode(double v);
+
 #ifdef __cplusplus
 }
 #endif

@@ -561,11 +561,140 @@ def pin_alltoall_layout(lib):
     assert sum(int(l["recv_displs"][-1]) for l in lay) == int(m.sum())
 
 
+# ------------------------------------------------------------------ MXFP4 quantiser
+# Pins of oracle_mxfp4_quant, the reading of the route+quant activation format taken
+# from the OCP Microscaling (MX) v1.0 MXFP4 format: E2M1 elements (1 sign, 2 exponent
+# bits with bias 1, 1 mantissa bit; exponent 0 is the subnormal range), 32-element
+# blocks, an E8M0 shared scale 2^(floor(log2 amax) - 2), round to nearest with ties to
+# the even code, saturation at the largest magnitude.
+
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit E2M1 code from its bit fields."""
+    sign = -1.0 if code & 8 else 1.0
+    ex, m = (code >> 1) & 3, code & 1
+    mag = 0.5 * m if ex == 0 else 2.0 ** (ex - 1) * (1.0 + 0.5 * m)
+    return sign * mag
+
+
+def e2m1_by_thresholds(v: float) -> int:
+    """Code by comparisons against the midpoints of consecutive magnitudes; at a midpoint
+    the neighbour whose code ends in 0 wins, so the test is > below an odd code and >=
+    below an even one."""
+    a = abs(v)
+    mag = (int(a > 0.25) + int(a >= 0.75) + int(a > 1.25) + int(a >= 1.75) + int(a > 2.5)
+           + int(a >= 3.5) + int(a > 5.0))
+    return (8 if np.signbit(v) else 0) | mag
+
+
+def pin_e2m1_codes(lib):
+    vals = [e2m1_value(c) for c in range(8)]
+    assert vals == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    grid = np.concatenate([np.arange(0, 8.0, 1.0 / 64), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0,
+                                                        6.0, 7.999, 100.0, 1e30]])
+    for v in grid:
+        for sv in (float(v), -float(v)):
+            got = oracle.e2m1_encode(sv, lib)
+            assert got == e2m1_by_thresholds(sv), (sv, got)
+            # nearest representable magnitude (saturating), brute force over the 8 codes
+            a = min(abs(sv), 6.0)
+            dist = [abs(a - abs(e2m1_value(c))) for c in range(8)]
+            assert dist[got & 7] == min(dist), (sv, got)
+    assert oracle.e2m1_encode(-0.0, lib) == 8 and oracle.e2m1_encode(0.0, lib) == 0
+    assert oracle.e2m1_encode(-0.1, lib) == 8 and oracle.e2m1_encode(-7.0, lib) == 15
+
+
+def _bf16(x):
+    return gen.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+
+
+def pin_mx_scale(lib):
+    rng = np.random.default_rng(21)
+    for j in range(-130, 128, 3):
+        # a block whose largest magnitude lies in [2^j, 2^(j+1)): scale exponent j - 2
+        amax = np.float32(2.0 ** j * (1.0 + rng.random() * 0.99))
+        if not np.isfinite(amax) or amax == 0:
+            continue
+        blk = (rng.random(32).astype(np.float32) * amax).astype(np.float32)
+        blk[rng.integers(32)] = -amax
+        xb = _bf16(blk).reshape(1, 32)
+        real = float(np.abs(gen.bf16_bits_to_f32(xb)).max())
+        if real == 0.0:
+            continue
+        want = min(max(int(np.floor(np.log2(real))) - 2, -127), 127)
+        got = int(oracle.mxfp4_quant(xb, lib)["scales"][0, 0])
+        assert got == want + 127, (j, real, got, want)
+    zero = np.zeros((1, 32), np.uint16)
+    zero[0, 5] = 0x8000  # -0
+    r = oracle.mxfp4_quant(zero, lib)
+    assert int(r["scales"][0, 0]) == 0 and int(r["q"][0, 2]) == 0x80
+    big = np.full((1, 32), 0x7F7F, np.uint16)  # the largest bf16, 2^127 * (2 - 2^-7)
+    assert int(oracle.mxfp4_quant(big, lib)["scales"][0, 0]) == 125 + 127
+
+
+def pin_mx_roundtrip(lib):
+    """Blocks of exact E2M1 multiples of 2^s with one element at +-4 or +-6 quantise to
+    exactly those codes and that scale."""
+    rng = np.random.default_rng(22)
+    for trial in range(300):
+        s = int(rng.integers(-120, 120))
+        codes = rng.integers(0, 16, 32)
+        codes[rng.integers(32)] = int(rng.choice([6, 7, 14, 15]))
+        vals = np.array([e2m1_value(int(c)) * 2.0 ** s for c in codes], dtype=np.float32)
+        xb = _bf16(vals).reshape(1, 32)
+        assert np.array_equal(gen.bf16_bits_to_f32(xb).ravel(), vals)  # exact in bf16
+        r = oracle.mxfp4_quant(xb, lib)
+        assert int(r["scales"][0, 0]) == s + 127
+        q = r["q"][0]
+        got = np.empty(32, np.int64)
+        got[0::2] = q & 0xF
+        got[1::2] = q >> 4
+        # +0 and -0 are the same value: compare values, and codes where nonzero
+        deq = np.array([e2m1_value(int(c)) for c in got])
+        want = np.array([e2m1_value(int(c)) for c in codes])
+        assert np.array_equal(deq, want), trial
+        nz = want != 0
+        assert np.array_equal(got[nz], codes[nz]), trial
+
+
+def pin_mx_nearest(lib):
+    """Every element of random blocks is the nearest (saturating) multiple of the scale."""
+    x = gen.f32_to_bf16_bits(gen.normal_f32(23, 8 * 256, std=3.0).reshape(8, 256))
+    r = oracle.mxfp4_quant(x, lib)
+    xf = gen.bf16_bits_to_f32(x).astype(np.float64)
+    for t in range(8):
+        for b in range(8):
+            e = int(r["scales"][t, b]) - 127
+            for i in range(32):
+                byte = int(r["q"][t, b * 16 + i // 2])
+                c = (byte >> 4) if i & 1 else (byte & 0xF)
+                v = xf[t, b * 32 + i] / 2.0 ** e
+                assert c == e2m1_by_thresholds(v), (t, b, i, v, c)
+
+
+def pin_mx_layout(lib):
+    """Element 2i in the low nibble of byte i of its block, block b at bytes 16b.., the
+    scale of block b of row t at t * H / 32 + b."""
+    H = 128
+    x = np.zeros((2, H), np.float32)
+    x[:, 0::32] = 6.0            # fixes every scale at 2^0
+    x[1, 33] = 1.0               # row 1, block 1, element 1: high nibble of byte 16
+    x[1, 66] = -0.5              # row 1, block 2, element 2: low nibble of byte 33
+    x[0, 127] = 5.5              # row 0, block 3, element 31: high nibble of byte 63 (-> 6)
+    r = oracle.mxfp4_quant(_bf16(x), lib)
+    assert np.all(r["scales"] == 127)
+    assert int(r["q"][1, 16]) == (0x2 << 4) | 0x7
+    assert int(r["q"][1, 33]) == 0x9
+    assert int(r["q"][0, 63]) == 0x7 << 4
+    assert int(r["q"][0, 0]) == 0x7 and int(r["q"][0, 1]) == 0
+    assert r["q"].shape == (2, H // 2) and r["scales"].shape == (2, H // 32)
+
+
 ALL_PINS = [
     pin_sigmoid_exact, pin_sigmoid_symmetry, pin_bf16_rounding, pin_selection_brute_force,
     pin_selection_exhaustive, pin_selection_kimi_shape, pin_plain_topk, pin_keep_all_groups_is_noop,
     pin_weights, pin_histogram_scan_perm, pin_invariants, pin_rank_local_matrix, pin_page_facts,
     pin_router_gemm, pin_rejects_invalid, pin_layout_inverse, pin_layout_tile_one, pin_layout_append,
     pin_layout_invariants, pin_layout_rejects, pin_route_index, pin_token_sharded,
-    pin_dispatch_counts, pin_alltoall_layout,
+    pin_dispatch_counts, pin_alltoall_layout, pin_e2m1_codes, pin_mx_scale, pin_mx_roundtrip,
+    pin_mx_nearest, pin_mx_layout,
 ]

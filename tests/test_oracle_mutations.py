@@ -60,6 +60,15 @@ MUTANTS = {
     "dispatch_interleaved_ranks": ("        send_counts[ids[i] / per] += 1;", "        send_counts[ids[i] % R] += 1;"),
     "alltoall_row_for_column": ("        recv_counts[s] = matrix[(size_t)s * R + me];",
                                 "        recv_counts[s] = matrix[(size_t)me * R + s];"),
+    "e2m1_ties_to_larger": ("if (dc < db || (dc == db && (c & 1) == 0)) best = c;",
+                            "if (dc <= db) best = c;"),
+    "e2m1_sign_dropped": ("int neg = signbit(v) ? 1 : 0;", "int neg = 0;"),
+    "mx_emax_three": ("e = (ex - 1) - 2;", "e = (ex - 1) - 3;"),
+    "mx_ceil_log2": ("e = (ex - 1) - 2;", "e = ex - 2;"),
+    "mx_zero_block_unit_scale": ("                e = -127;\n            } else {",
+                                 "                e = 0;\n            } else {"),
+    "mx_no_low_clamp": ("if (e < -127) e = -127;", "if (e < -200) e = -200;"),
+    "mx_nibbles_swapped": ("(uint8_t)(lo | (hi << 4));", "(uint8_t)(hi | (lo << 4));"),
 }
 
 # cheap pins first; the exhaustive sigmoid sweep last
