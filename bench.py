@@ -222,29 +222,40 @@ def to_dev_bf16(torch, arr, dev):
 
 def decode_latency(torch, mr, dev, reps=200, replays=10):
     """µs per call under CUDA-graph replay (rank-local ids, offset 336, count 112),
-    against an empty kernel with the same launch shape replayed the same way."""
-    res = {"T": [], "ctas": [], "us_per_call": [], "floor_us": [], "ratio_to_floor": []}
+    against an empty kernel with the same launch shape replayed the same way; also the
+    fused route+quant launch (the same routing plus the MXFP4 quantisation of the batch's
+    bf16 activations [T, 7168])."""
+    res = {"T": [], "ctas": [], "us_per_call": [], "floor_us": [], "ratio_to_floor": [],
+           "route_quant_us_per_call": []}
     st = torch.cuda.Stream(device=dev)
     for T in (8, 16, 24, 32, 64):
         cfg = gen.cfg1(T)
         lg = to_dev_bf16(torch, cfg["logits"], dev)
         bias = torch.from_numpy(cfg["bias"]).to(dev)
+        x = to_dev_bf16(torch, gen.mx_activations(T), dev)
         out = mr.alloc_outputs(T, E, K, 112, dev)
+        outq = mr.alloc_outputs(T, E, K, 112, dev)
         ctas = mr.decode_ctas(T)  # the routing launch's cluster
         with torch.cuda.stream(st):
             mr.route(lg, bias, local_offset=336, local_count=112, out=out, stream=st)
+            mr.route_quant(lg, bias, x, local_offset=336, local_count=112, out=outq, stream=st)
             mr.empty_kernel(ctas, stream=st)
             st.synchronize()
             g_route = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_route, stream=st):
                 for _ in range(reps):
                     mr.route(lg, bias, local_offset=336, local_count=112, out=out, stream=st)
+            g_quant = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_quant, stream=st):
+                for _ in range(reps):
+                    mr.route_quant(lg, bias, x, local_offset=336, local_count=112, out=outq,
+                                   stream=st)
             g_empty = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_empty, stream=st):
                 for _ in range(reps):
                     mr.empty_kernel(ctas, stream=st)
         times = {}
-        for name, g in (("route", g_route), ("empty", g_empty)):
+        for name, g in (("route", g_route), ("quant", g_quant), ("empty", g_empty)):
             with torch.cuda.stream(st):  # replay and time on the same stream
                 g.replay()
                 st.synchronize()
@@ -263,6 +274,7 @@ def decode_latency(torch, mr, dev, reps=200, replays=10):
         res["us_per_call"].append(round(times["route"], 3))
         res["floor_us"].append(round(times["empty"], 3))
         res["ratio_to_floor"].append(round(times["route"] / times["empty"], 3))
+        res["route_quant_us_per_call"].append(round(times["quant"], 3))
     return res
 
 

@@ -213,5 +213,36 @@ def cfg_decision_edges(kind: str, T: int = 3000, E: int = E_KIMI, off: int = 0, 
     return dict(base, logits=logits, bias=bias)
 
 
+def mx_activations(T: int, H: int = H_KIMI, kind: str = "normal", seed: int = 12) -> np.ndarray:
+    """bf16 activations [T, H] for the fused route+quant launch:
+      normal    N(0,1) (seed 12), the decode batch's hidden states;
+      patterns  bf16 bit patterns drawn uniformly (seed 13), non-finite ones made finite by
+                clearing the top exponent bit: zeros, subnormals, huge and tiny values;
+      ties      blocks of 32 whose elements sit on the midpoints between E2M1 magnitudes
+                (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) or in (6, 8), times 2^s, with 7 * 2^s
+                in each block (so that the block scale is 2^s), random signs and s
+                (seed 14); every fourth block all zeros.
+    """
+    if kind == "normal":
+        return f32_to_bf16_bits(normal_f32(seed, T * H).reshape(T, H))
+    if kind == "patterns":
+        h = (raw64(13, T * H) >> np.uint64(48)).astype(np.uint16)
+        bad = (h & np.uint16(0x7F80)) == np.uint16(0x7F80)
+        h[bad] ^= np.uint16(0x4000)
+        return h.reshape(T, H)
+    if kind == "ties":
+        nb = T * H // 32
+        mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.5, 7.5, 6.0, 0.0])
+        pick = (raw64(14, nb * 32, sub=1) % np.uint64(mids.size)).astype(np.int64).reshape(nb, 32)
+        vals = mids[pick]
+        vals[:, 0] = 7.0
+        sign = np.where((raw64(14, nb * 32, sub=2) & np.uint64(1)).reshape(nb, 32) == 1, -1.0, 1.0)
+        s = (raw64(14, nb, sub=3) % np.uint64(200)).astype(np.int64) - 100
+        v = (vals * sign * np.exp2(s.astype(np.float64))[:, None]).astype(np.float32)
+        v[::4] = 0.0
+        return f32_to_bf16_bits(v.reshape(T, H))
+    raise ValueError(kind)
+
+
 def num_local_experts(E: int, ep: int) -> int:
     return E // ep

@@ -98,6 +98,35 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
               int32_t* topk_ids, struct CUstream_st* stream);
 
 /*
+ * moe_route_quant -- the fused route+quant decode launch: moe_route for a decode batch of
+ * T <= MOE_ROUTE_QUANT_MAX_TOKENS rows and, in the same kernel launch, the MXFP4
+ * quantisation of the batch's activations x that the routed MXFP4 MoE consumes.  The
+ * page's fused launch (sglang PR #37, Rank-local expert ids for the EP routed MoE,
+ * description: route_quant_fused handles decode batches up to MAX_TOKENS = 64 tokens
+ * and writes the packed ids the MXFP4 routed MoE reads) does not define the activation
+ * format; the reading taken is the MXFP4 format of the OCP Microscaling Formats (MX)
+ * specification v1.0:
+ *   per block of 32 consecutive elements of a row, e = floor(log2 max |x|) - 2 clamped
+ *   to [-127, 127] (-127 for a block of zeros); x_scales holds the E8M0 byte e + 127;
+ *   each element x / 2^e is rounded to E2M1 (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6) to
+ *   nearest, ties to the code whose last bit is 0, magnitudes above 6 saturated, the
+ *   sign kept (code bit 3); x_q holds two codes per byte, the even element in the low
+ *   nibble.
+ *   x         [T, H] bf16 bits, 16-byte aligned, finite; H % 32 == 0.
+ *   x_q       [T, H / 2] bytes out, 2-byte aligned; x_scales [T, H / 32] bytes out.
+ *   Routing arguments and outputs are those of moe_route (same results).
+ * Errors: those of moe_route; INVALID_ARG for H <= 0, H % 32 != 0, NULL x / x_q /
+ * x_scales with T > 0, or misaligned x / x_q; UNSUPPORTED for T > 64.  One kernel launch
+ * (a programmatic dependent, like moe_route for T <= 64 rows).
+ */
+#define MOE_ROUTE_QUANT_MAX_TOKENS 64
+int moe_route_quant(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+                    int n_group, int topk_group, float scale, int local_offset, int local_count,
+                    const uint16_t* x, int H, uint8_t* x_q, uint8_t* x_scales, int32_t* packed,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* topk_ids,
+                    struct CUstream_st* stream);
+
+/*
  * moe_router_gemm_route -- router contraction a0 fused in front of moe_route:
  *   logits[t][e] = sum_h hidden[t][h] * w_router[e][h], bf16 inputs, fp32 accumulate,
  * then steps a1..a11 on those fp32 logits.  The router weight is 896 x 7168 per layer

@@ -50,6 +50,8 @@ def load(path: str | None = None):
     lib.moe_route.restype = I
     lib.moe_router_gemm_route.argtypes = [P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
     lib.moe_router_gemm_route.restype = I
+    lib.moe_route_quant.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P, P, P]
+    lib.moe_route_quant.restype = I
     lib.moe_route_host.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P]
     lib.moe_route_host.restype = I
     lib.moe_route_host_release.argtypes = []
@@ -177,6 +179,36 @@ def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int
                           _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]),
                           _ptr(out.get("ids")), _stream(stream))
     _check(rc, "moe_route")
+    return out
+
+
+QUANT_MAX_TOKENS = 64
+
+
+def route_quant(logits: torch.Tensor, bias: torch.Tensor, x: torch.Tensor, *, k: int = 16,
+                n_group: int = 8, topk_group: int = 4, scale: float = 2.5, local_offset: int = 0,
+                local_count: int = 0, out: dict | None = None, want_ids: bool = False,
+                stream=None) -> dict:
+    """moe_route_quant: routing of a decode batch (T <= 64) and, in the same launch, the
+    MXFP4 codes (out["x_q"], uint8 [T, H / 2]) and E8M0 scales (out["x_scales"], uint8
+    [T, H / 32]) of the activations x (bfloat16 [T, H] on the device)."""
+    if not (logits.is_cuda and bias.is_cuda and x.is_cuda):
+        raise ValueError("logits, bias and x must be CUDA tensors")
+    if x.dtype != torch.bfloat16 or not x.is_contiguous() or x.dim() != 2:
+        raise ValueError("x must be a contiguous bfloat16 [T, H] tensor")
+    T, E = logits.shape
+    H = x.shape[1]
+    if out is None:
+        out = alloc_outputs(T, E, k, local_count, logits.device, want_ids)
+    if "x_q" not in out:
+        out["x_q"] = torch.empty((T, H // 2), dtype=torch.uint8, device=logits.device)
+        out["x_scales"] = torch.empty((T, H // 32), dtype=torch.uint8, device=logits.device)
+    rc = load().moe_route_quant(_ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group,
+                                topk_group, float(scale), local_offset, local_count, _ptr(x), H,
+                                _ptr(out["x_q"]), _ptr(out["x_scales"]), _ptr(out["packed"]),
+                                _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]),
+                                _ptr(out.get("ids")), _stream(stream))
+    _check(rc, "moe_route_quant")
     return out
 
 

@@ -219,6 +219,52 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
   return ce == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }
 
+int moe_route_quant(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+                    int n_group, int topk_group, float scale, int local_offset, int local_count,
+                    const uint16_t* x, int H, uint8_t* x_q, uint8_t* x_scales, int32_t* packed,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* topk_ids,
+                    struct CUstream_st* stream) {
+  int rc = check_route_args(T, E, k, n_group, topk_group, local_offset, local_count);
+  if (rc != MOE_ROUTE_OK) return rc;
+  if (logits_dtype != MOE_ROUTE_F32 && logits_dtype != MOE_ROUTE_BF16) return MOE_ROUTE_E_INVALID_ARG;
+  if (!bias || !counts || !offsets) return MOE_ROUTE_E_INVALID_ARG;
+  if (T > 0 && (!logits || !packed || !perm || !x || !x_q || !x_scales)) return MOE_ROUTE_E_INVALID_ARG;
+  if (H <= 0 || H % 32 != 0) return MOE_ROUTE_E_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(logits) % 16 != 0 || reinterpret_cast<uintptr_t>(bias) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(x_q) % 2 != 0)
+    return MOE_ROUTE_E_INVALID_ARG;
+  if (T > MOE_ROUTE_QUANT_MAX_TOKENS) return MOE_ROUTE_E_UNSUPPORTED;
+  if (static_cast<long long>(T) * H >= (1ll << 31)) return MOE_ROUTE_E_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DevState* d = nullptr;
+  rc = get_state(st, &d);
+  if (rc != MOE_ROUTE_OK) return rc;
+  RouteArgs a = {};
+  a.logits = logits;
+  a.bias = bias;
+  a.stab = d->stab;
+  a.etab = d->etab;
+  a.packed = packed;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.perm = perm;
+  a.ids = topk_ids;
+  a.err = d->err;
+  a.T = T;
+  a.k = k;
+  a.Kg = topk_group;
+  a.off = local_offset;
+  a.cnt = local_count;
+  a.NE = bins(E, k, local_count);
+  a.scale = scale;
+  a.qx = x;
+  a.qcodes = x_q;
+  a.qscales = x_scales;
+  a.qH = H;
+  const int dt = logits_dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32;
+  return launch_route_decode(a, dt, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
+}
+
 int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, const float* bias,
                           int T, int H, int E, int k, int n_group, int topk_group, float scale,
                           int local_offset, int local_count, float* logits_out, int32_t* packed,

@@ -92,8 +92,68 @@ __device__ __forceinline__ void mask_count_scan(const unsigned long long* mask, 
   __syncthreads();
 }
 
-// SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).
-template <int DT, bool SPEC>
+// --------------------------------------------------------- MXFP4 quantisation
+// The quant half of the fused route+quant decode launch: the batch's activations
+// x [T, H] (bf16) become MXFP4 (OCP Microscaling v1.0 MXFP4, the format the routed MXFP4
+// MoE consumes; sglang PR #37, description: route_quant_fused, decode batches up to 64
+// tokens).  Per block of 32 consecutive elements of a row: scale exponent
+// e = floor(log2 max |x|) - 2, clamped to [-127, 127] (-127 for a block of zeros), stored
+// as the E8M0 byte e + 127; elements x / 2^e rounded to E2M1 to nearest, ties to even,
+// saturating at 6, by the hardware conversion; two codes per byte, even element low.
+
+// E2M1 codes of two floats: lo in bits 0-3, hi in bits 4-7.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Quantises blocks gw * 4 + 4 i * GW + (0..3) of the batch (warp gw of GW): lanes 8j..8j+7
+// take block j of a group of four, four elements each.
+__device__ __forceinline__ void mxfp4_quant_blocks(const RouteArgs& a, int gw, int GW) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int nbr = a.qH >> 5;  // blocks per row
+  const int nblk = a.T * nbr;
+  const int sub = lane & 7;
+  for (int b0 = gw * 4; b0 < nblk; b0 += GW * 4) {
+    const int b = b0 + (lane >> 3);
+    const bool act = b < nblk;
+    const int t = act ? b / nbr : 0;
+    const int c = act ? b - t * nbr : 0;
+    uint2 v = make_uint2(0u, 0u);
+    if (act) v = __ldg(reinterpret_cast<const uint2*>(a.qx + size_t(t) * a.qH + c * 32 + sub * 4));
+    // the block's largest magnitude, as bf16 magnitude bits (they order like the values)
+    uint32_t m = max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu));
+    m = max(m, __shfl_xor_sync(FULL, m, 1));
+    m = max(m, __shfl_xor_sync(FULL, m, 2));
+    m = max(m, __shfl_xor_sync(FULL, m, 4));
+    int e = -127;
+    if (m != 0u) {
+      // floor(log2 amax): the exponent field, or for a subnormal the leading mantissa bit
+      const int ex = int(m >> 7);
+      const int fl = ex > 0 ? ex - 127 : -133 + (31 - __clz(int(m)));
+      e = min(max(fl - 2, -127), 127);
+    }
+    const float inv = __int_as_float(uint32_t(127 - e) << 23);  // 2^-e (e <= 125 for bf16)
+    const float f0 = __fmul_rn(__uint_as_float(v.x << 16), inv);
+    const float f1 = __fmul_rn(__uint_as_float(v.x & 0xFFFF0000u), inv);
+    const float f2 = __fmul_rn(__uint_as_float(v.y << 16), inv);
+    const float f3 = __fmul_rn(__uint_as_float(v.y & 0xFFFF0000u), inv);
+    const uint32_t bytes = e2m1x2(f0, f1) | (e2m1x2(f2, f3) << 8);
+    if (act) {
+      *reinterpret_cast<uint16_t*>(a.qcodes + size_t(t) * (a.qH >> 1) + c * 16 + sub * 2) =
+          static_cast<uint16_t>(bytes);
+      if (sub == 0) a.qscales[size_t(t) * nbr + c] = static_cast<uint8_t>(e + 127);
+    }
+  }
+}
+
+// SPEC: k = 16 and topk_group = 4 compiled in (the Kimi-K3 instance).  QUANT: the
+// launch also quantises the activations a.qx (moe_route_quant).
+template <int DT, bool SPEC, bool QUANT = false>
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a) {
   using L = DecodeSmem<DT>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -146,6 +206,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
              uint32_t(nrows) * L::ROWB, mbar);
   }
+  // the activations' quantisation overlaps the row copies in flight
+  if constexpr (QUANT) mxfp4_quant_blocks(a, crank * kDecodeRowsPerCta + w, nctas * kDecodeRowsPerCta);
   if (have) mbar_wait_bounded(mbar, 0, a.err);
 
   SlotOut o = {};
@@ -293,12 +355,12 @@ cudaError_t launch_empty(int ctas, cudaStream_t st) {
 }
 
 // Shared-memory size of one decode kernel; clears *wide if clusters of 16 are refused.
-template <int DT, bool SPEC>
+template <int DT, bool SPEC, bool QUANT = false>
 static cudaError_t set_decode_smem(bool* wide) {
-  cudaError_t e = cudaFuncSetAttribute(k_route_decode<DT, SPEC>,
+  cudaError_t e = cudaFuncSetAttribute(k_route_decode<DT, SPEC, QUANT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, DecodeSmem<DT>::total);
   if (e != cudaSuccess) return e;
-  if (cudaFuncSetAttribute(k_route_decode<DT, SPEC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+  if (cudaFuncSetAttribute(k_route_decode<DT, SPEC, QUANT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
       cudaSuccess) {
     cudaGetLastError();
     *wide = false;
@@ -316,6 +378,10 @@ cudaError_t setup_decode_kernels() {
   if ((e = set_decode_smem<DT_SCORE, false>(&wide)) != cudaSuccess) return e;
   if ((e = set_decode_smem<DT_SCORE, true>(&wide)) != cudaSuccess) return e;
   if ((e = set_decode_smem<DT_PACKED, false>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_F32, false, true>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_F32, true, true>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_BF16, false, true>(&wide)) != cudaSuccess) return e;
+  if ((e = set_decode_smem<DT_BF16, true, true>(&wide)) != cudaSuccess) return e;
   if (cudaFuncSetAttribute(k_empty, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
     wide = false;
@@ -345,6 +411,9 @@ cudaError_t setup_decode_kernels() {
 template <int DT, bool SPEC>
 static cudaError_t launch_decode_t(cudaLaunchConfig_t& cfg, const RouteArgs& a) {
   cfg.dynamicSmemBytes = DecodeSmem<DT>::total;
+  if constexpr (DT == DT_BF16 || DT == DT_F32) {
+    if (a.qx != nullptr) return cudaLaunchKernelEx(&cfg, k_route_decode<DT, SPEC, true>, a);
+  }
   return cudaLaunchKernelEx(&cfg, k_route_decode<DT, SPEC>, a);
 }
 

@@ -41,6 +41,12 @@ struct RouteArgs {
                                             // persistent kernels
   int barrier_skip_cta = -1;  // CTA that leaves before the first grid barrier (-1: none;
                               // a test of the timeout path)
+  // MXFP4 quantisation of the decode batch's activations in the same launch
+  // (moe_route_quant); unused when qx is null
+  const uint16_t* qx = nullptr;  // [T, qH] bf16 bits
+  uint8_t* qcodes = nullptr;     // [T, qH / 2] two E2M1 codes per byte, even element low
+  uint8_t* qscales = nullptr;    // [T, qH / 32] E8M0
+  int qH = 0;
 };
 
 // Per-warp shared scratch of the row routine.  NB = biased scores parked by the kept
