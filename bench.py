@@ -70,7 +70,8 @@ def measured_peaks():
 
 # the sources k_route_prefill is compiled from: the recorded DRAM traffic stays valid
 # while none of them changes
-PREFILL_SOURCES = ("common.cuh", "launch.h", "route_prefill.cu", "route_row.cuh")
+PREFILL_SOURCES = ("common.cuh", "launch.h", "persist.cuh", "route_pair.cuh", "route_prefill_fast.cu",
+                   "route_row.cuh")
 
 
 def csrc_hash():
@@ -563,7 +564,7 @@ def main():
         "hbm_gbs": ab / (ms_per_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "k_route_prefill<bf16>", "algorithmic_bytes": ab,
+                     "kernel": "k_route_prefill_fast", "algorithmic_bytes": ab,
                      "kernel_us": kernel_ms * 1e3, "peak_source": f"{peak_src} hbm_gbs (copy)"},
         "clocks": clocks,
         "e2e": ({"value": world * T_PREFILL / (e2e_ms * 1e-3), "unit": "tokens/s",

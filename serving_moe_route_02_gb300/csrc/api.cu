@@ -19,7 +19,7 @@ struct DevState {
   int nsm = 0;
   int blocks_per_sm = 0;
   int fast_blocks_per_sm = 0;  // the approximate-score persistent kernel
-  float eps_half = 0.0f;       // its measured approximation bound (route_fast.cuh)
+  float eps_half = 0.0f;       // its measured approximation bound (route_pair.cuh)
   float* stab = nullptr;  // sigmoid table for bf16 logits
   float2* etab = nullptr; // 2^(j/64) table for float32 logits
   int* err = nullptr;     // device status word

@@ -57,7 +57,7 @@ cudaError_t setup_prefill_fast(int* blocks_per_sm);
 bool prefill_fast_fits(int T, int grid);
 cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, int grid,
                                       cudaStream_t st);
-// Writes the bits of E_half (route_fast.cuh) to *out, which must hold 0.
+// Writes the bits of E_half (route_pair.cuh) to *out, which must hold 0.
 cudaError_t launch_approx_err(unsigned* out, cudaStream_t st);
 // The argument checks of moe_route (status code; MOE_ROUTE_OK when the call is valid).
 int route_args_status(int T, int E, int k, int n_group, int topk_group, int off, int cnt);

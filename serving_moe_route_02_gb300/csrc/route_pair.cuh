@@ -2,34 +2,62 @@
 // Kimi-K3 instance): lanes 0-15 route the first row, lanes 16-31 the second.  The result
 // is identical to route_row's.
 //
+// Why approximate scores.  The exact score of a bf16 logit is a table lookup (common.cuh)
+// whose index depends on the data, so a warp's 32 lookups fall on shared-memory banks
+// unevenly (about 3.5-way conflicts); for all 896 experts of a row that is the costliest
+// part of routing.  Here every expert first gets a cheap approximate score, and the exact
+// table is read only for the experts a decision depends on (about 18 of 896 per row), or
+// for a whole row in the rare cases listed below.
+//
 // Layout.  Lane h of a half (h = lane & 15) owns the 56 experts [56 h, 56 h + 56) as two
 // "chains" of 28: chain a = [56 h, 56 h + 28) and chain b = [56 h + 28, 56 h + 56), each a
 // quarter of a group of 112; a group is lanes 2g and 2g + 1.  Approximate scores are kept
 // as packed f16 pairs: word j holds element j of chain a (low half) and of chain b (high
 // half), so one packed max/min step tracks the two largest values of both chains at once.
 //
-// Approximate scores (see route_fast.cuh for the exact-score fallbacks and the argument
-// that the survivors contain the exact top k):
+// Approximate scores:
 //   b'' = f16(fma(0.5, tanh.approx(x / 2), c'')),  c'' = bias + (0.5 - o),
 // where o centres the values (|b''| <= R = (bias_max - bias_min + 1) / 2), so the f16
 // rounding error is at most half an f16 ulp at R.  With the offset added back, b'' + o is
 // within eps of the exact b = s + bias:
-//   eps = E_half + ulp_f16(R) / 2 + (2 + B) 2^-22 + 2^-24,   B = max |bias|.
+//   eps = E_half + ulp_f16(R) / 2 + (2 + B) 2^-22 + 2^-24,   B = max |bias|,
+// where E_half bounds |0.5 tanh.approx(x / 2) - (sigmoid(x) - 0.5)| over every bf16 input
+// (measured exhaustively on the device when the library state is created; about 3.5e-6
+// on sm_103a) and the other terms cover the roundings of the additions.  A group score is
+// fl(m1 + m2) of the group's two largest b, so its approximate value is within
+// delta = 2 eps + (2 + 2B) 2^-22 of the exact one.
 // Steps per row (everything in the row's half-warp):
-//   group scores from the chains' two largest values; kept groups certain when the 4th
-//     and 5th group scores differ by more than 2 delta, else exact group scores;
-//   p16 = the 16th largest of the 32 kept chains' top-2 values (a bitonic sort of packed
-//     f16 pairs across the half); survivors: kept experts with b'' >= p16 - 2 eps
-//     (packed compares give a bit per expert), compacted in ascending id order;
-//   exact scores of the survivors (table lookups, two per lane) and a bitonic sort of
-//     their 32-bit keys (exact b, then id) gives slots 0..15;
+//   group choice: the 4th and 5th approximate group scores differ by more than 2 delta,
+//     so the kept set is certain; otherwise (about one row in 100) the exact group scores
+//     are computed from the table;
+//   top-k: p16 = the 16th largest of the 32 kept chains' top-2 values (a bitonic sort of
+//     packed f16 pairs across the half).  At least 16 kept experts have b'' >= p16, so the
+//     exact 16th largest tau satisfies tau >= p16 + o - eps, and every kept expert whose
+//     exact b reaches tau has b'' >= p16 - 2 eps; every other expert has exact b < tau.
+//     The experts with b'' >= p16 - 2 eps ("survivors", 17-22 on the prefill workload,
+//     always at least 16) get packed compares (a bit per expert), are compacted in
+//     ascending id order, looked up in the exact table (two per lane) and ranked by a
+//     bitonic sort of 32-bit keys (exact b, then id), which gives slots 0..15;
 //   weights from the exact scores in slot order, relabel, pack.
 // Rare cases: more than 32 survivors in a row, or keys that do not fit 32 bits, take an
 // exact extraction (16 rounds of a half-warp maximum over the survivors).
 #pragma once
-#include "route_fast.cuh"
+#include "route_row.cuh"
 
 namespace moe {
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// a - b and a + b rounded toward -infinity
+__device__ __forceinline__ float fsub_down(float a, float b) {
+  float y;
+  asm("sub.rm.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
 
 constexpr int kPairEPL = 56;   // experts per lane
 constexpr int kChain = 28;     // experts per chain

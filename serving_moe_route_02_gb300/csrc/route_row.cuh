@@ -36,7 +36,7 @@ struct RouteArgs {
   int T, k, Kg, off, cnt, NE;
   float scale;
   float eps_half;         // bound on |0.5 tanh.approx(x / 2) - (sigmoid(x) - 0.5)| over
-                          // bf16 x, measured on the device (route_fast.cuh)
+                          // bf16 x, measured on the device (route_pair.cuh)
   uint64_t barrier_wait_ns = kWaitLimitNs;  // limit of each grid-barrier wait of the
                                             // persistent kernels
   int barrier_skip_cta = -1;  // CTA that leaves before the first grid barrier (-1: none;

@@ -291,6 +291,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   __syncthreads();
+  // no CTA leaves while a peer's copies may still target its shared memory (after a
+  // wait that ran out above, incoming copies can still be in flight); every earlier wait
+  // is bounded and every CTA reaches this point
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------- host side
