@@ -289,13 +289,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   }
-  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (threadIdx.x == 0) {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    // After the receive wait ran out, a peer's copy into this CTA's shared memory may
+    // still be on its way: every peer sends unconditionally once its own bounded waits
+    // (at most kMaxStages + 2 of them) are over, so waiting that long again covers it;
+    // the CTA does not leave while a copy can still land.
+    if (!recv_ok) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(recv_bar, 0) && globaltimer_ns() - t0 < (kMaxStages + 3) * kWaitLimitNs) {
+      }
+    }
+  }
   __syncthreads();
-  // no CTA leaves while a peer's copies may still target its shared memory (after a
-  // wait that ran out above, incoming copies can still be in flight); every earlier wait
-  // is bounded and every CTA reaches this point
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------- host side
