@@ -316,7 +316,7 @@ def gemm_route_latency(torch, mr, dev, reps=100, replays=10):
     return res
 
 
-def layout_timing(torch, mr, dev, out, T, tile=128, reps=50, replays=10):
+def layout_timing(torch, mr, dev, out, T, tile=128, reps=50, replays=10, bufs=None, bias=None):
     """moe_route_layout at T rows (global ids): µs per call under CUDA-graph replay (so
     that host-side call overhead does not hide the kernel), with and without the inverse
     permutation, and the HBM bandwidth of its algorithmic bytes (perm read once, inverse
@@ -352,11 +352,34 @@ def layout_timing(torch, mr, dev, out, T, tile=128, reps=50, replays=10):
 
     us = replay_us(L)
     us_padded = replay_us(dict(L, inv_perm=None))
+    # the inverse map written by the routing instead (moe_route_ex): its extra cost per
+    # 65,536-row routing call, plain launches over the rotating input buffers
+    extra = None
+    if bufs is not None:
+        inv = torch.empty(T * K, dtype=torch.int32, device=dev)
+        outx = mr.alloc_outputs(T, E, K, 0, dev)
+
+        def route_us(with_inv, n=30):
+            o = dict(outx, inv_perm=inv if with_inv else None)
+            for i in range(3):
+                mr.route(bufs[i % len(bufs)], bias, out=o)
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(n):
+                mr.route(bufs[i % len(bufs)], bias, out=o)
+            b.record()
+            b.synchronize()
+            return a.elapsed_time(b) * 1e3 / n
+
+        extra = round(route_us(True) - route_us(False), 3)
     nbytes = 4 * n + 4 * n + 2 * 4 * cap + 4 * (2 * NE + 1) + 4 * (NE + 1)
     peaks, _ = measured_peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"T": T, "tile": tile, "capacity": cap, "us_per_call": round(us, 3),
-            "us_per_call_without_inverse": round(us_padded, 3), "timing": "CUDA-graph replay",
+            "us_per_call_without_inverse": round(us_padded, 3),
+            "routing_extra_us_for_inverse": extra, "timing": "CUDA-graph replay",
             "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
             "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
 
@@ -541,7 +564,7 @@ def main():
     if rank == 0 and not (args.no_decode or args.quick):
         decode = decode_latency(torch, mr, dev)
         gemm = gemm_route_latency(torch, mr, dev)
-        layout = layout_timing(torch, mr, dev, outs[0], T_PREFILL)
+        layout = layout_timing(torch, mr, dev, outs[0], T_PREFILL, bufs=bufs, bias=bias)
 
     peaks, peak_src = measured_peaks()
     ab = algorithmic_bytes(T_PREFILL)

@@ -98,6 +98,22 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
               int32_t* topk_ids, struct CUstream_st* stream);
 
 /*
+ * moe_route_ex -- moe_route with one more optional output:
+ *   inv_perm  [T * k] int32 out, nullable: inv_perm[t * k + j] = the position of entry
+ *             (t, j) in perm, i.e. perm[inv_perm[i]] = i (the inverse permutation).
+ * The routing kernels know each entry's place when they write perm and store it here in
+ * token order, so the stores are coalesced; moe_route_layout then need not build the
+ * inverse map (pass its inv_perm as NULL).  The routed entries reach the expert GEMMs in
+ * the routing's order (sglang PR #37, Rank-local expert ids for the EP routed MoE,
+ * description), and the combine step that brings each entry's result back to its token
+ * reads this map.  Everything else, including the errors, is as moe_route.
+ */
+int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+                 int n_group, int topk_group, float scale, int local_offset, int local_count,
+                 int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 int32_t* topk_ids, int32_t* inv_perm, struct CUstream_st* stream);
+
+/*
  * moe_route_quant -- the fused route+quant decode launch: moe_route for a decode batch of
  * T <= MOE_ROUTE_QUANT_MAX_TOKENS rows and, in the same kernel launch, the MXFP4
  * quantisation of the batch's activations x that the routed MXFP4 MoE consumes.  The
@@ -176,6 +192,9 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
  * perm with T * k > 0), a capacity below the bound, or a bound beyond 2^31 - 1;
  * UNSUPPORTED for NE > 1,056.  All outputs NULL: returns OK and enqueues nothing.
  * One kernel launch; no allocation after the library's per-device state exists.
+ * The inverse map costs one scattered 4-byte store per entry here; moe_route_ex writes
+ * the same map from the routing kernels in token order, so a caller that routes with
+ * moe_route_ex passes inv_perm = NULL here.
  */
 int moe_route_layout(const int32_t* counts, const int32_t* offsets, const int32_t* perm, int T,
                      int k, int NE, int tile, int32_t* inv_perm, int32_t* padded_offsets,

@@ -48,6 +48,8 @@ def load(path: str | None = None):
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.moe_route.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P]
     lib.moe_route.restype = I
+    lib.moe_route_ex.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
+    lib.moe_route_ex.restype = I
     lib.moe_router_gemm_route.argtypes = [P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
     lib.moe_router_gemm_route.restype = I
     lib.moe_route_quant.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P, P, P]
@@ -165,8 +167,11 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int = 8,
           topk_group: int = 4, scale: float = 2.5, local_offset: int = 0, local_count: int = 0,
-          out: dict | None = None, want_ids: bool = False, stream=None) -> dict:
-    """moe_route on a [T, E] CUDA tensor of router logits (float32 or bfloat16)."""
+          out: dict | None = None, want_ids: bool = False, want_inv: bool = False,
+          stream=None) -> dict:
+    """moe_route on a [T, E] CUDA tensor of router logits (float32 or bfloat16); with
+    want_inv (or an "inv_perm" tensor in out) moe_route_ex, which also writes the inverse
+    permutation out["inv_perm"]."""
     if not (logits.is_cuda and bias.is_cuda):
         raise ValueError("logits and bias must be CUDA tensors")
     if not logits.is_contiguous() or not bias.is_contiguous() or bias.dtype != torch.float32:
@@ -174,6 +179,16 @@ def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int
     T, E = logits.shape
     if out is None:
         out = alloc_outputs(T, E, k, local_count, logits.device, want_ids)
+    if want_inv and out.get("inv_perm") is None:
+        out["inv_perm"] = torch.empty(T * k, dtype=torch.int32, device=logits.device)
+    if out.get("inv_perm") is not None:
+        rc = load().moe_route_ex(_ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group,
+                                 topk_group, float(scale), local_offset, local_count,
+                                 _ptr(out["packed"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+                                 _ptr(out["perm"]), _ptr(out.get("ids")), _ptr(out["inv_perm"]),
+                                 _stream(stream))
+        _check(rc, "moe_route_ex")
+        return out
     rc = load().moe_route(_ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group,
                           topk_group, float(scale), local_offset, local_count, _ptr(out["packed"]),
                           _ptr(out["counts"]), _ptr(out["offsets"]), _ptr(out["perm"]),

@@ -152,6 +152,14 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
               int n_group, int topk_group, float scale, int local_offset, int local_count,
               int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
               int32_t* topk_ids, struct CUstream_st* stream) {
+  return moe_route_ex(logits, logits_dtype, bias, T, E, k, n_group, topk_group, scale, local_offset,
+                      local_count, packed, counts, offsets, perm, topk_ids, nullptr, stream);
+}
+
+int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+                 int n_group, int topk_group, float scale, int local_offset, int local_count,
+                 int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 int32_t* topk_ids, int32_t* inv_perm, struct CUstream_st* stream) {
   int rc = check_route_args(T, E, k, n_group, topk_group, local_offset, local_count);
   if (rc != MOE_ROUTE_OK) return rc;
   if (logits_dtype != MOE_ROUTE_F32 && logits_dtype != MOE_ROUTE_BF16) return MOE_ROUTE_E_INVALID_ARG;
@@ -174,6 +182,7 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
   a.offsets = offsets;
   a.perm = perm;
   a.ids = topk_ids;
+  a.inv = inv_perm;
   a.err = d->err;
   a.T = T;
   a.k = k;

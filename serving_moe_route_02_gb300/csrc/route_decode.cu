@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     const int t = row0 + w;
     const int pos = offs_s[o.lid] + __popcll(mask_s[o.lid] & ((1ull << t) - 1ull));
     a.perm[pos] = t * a.k + lane;
+    if (a.inv) a.inv[t * a.k + lane] = pos;
   }
 }
 

@@ -334,6 +334,9 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
     } else {
       a.perm[base_s[l] + rk] = x;
     }
+    // entry x's place in perm; the walk visits entries in token order, so these stores
+    // are coalesced row by row
+    if (a.inv) a.inv[x] = base_s[l] + rk;
   };
   for (int c0 = 0; c0 < nw; c0 += chunk_rows) {
     if (!keep && nchunks > 1) stage_chunk(c0);

@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     gbase_s[e] = __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
   }
   __syncthreads();
-  int* off_s = reinterpret_cast<int*>(smem + L::o_ent);  // the entries are placed: reuse
+  int* off_s = reinterpret_cast<int*>(smem + L::o_ws);  // the routing scratch is free
   block_scan_fast(hist_s, off_s, a.NE, tmp);
   if (cta == 0) {
     for (int e = tid; e < a.NE; e += NT) {
@@ -262,6 +262,16 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   __syncthreads();
   const int nvalid = lbase_s[a.NE];
   for (int i = tid; i < nvalid; i += NT) a.perm[gbase_s[sbin[i]] + i] = sval[i];
+  if (a.inv) {
+    // each entry's place in perm, in token order (coalesced): warp prefix + rank within
+    // the warp give its CTA-local position, gbase the rest
+    for (int x = lane; x < nrouted * K; x += 32) {
+      const uint32_t v = ent[x];
+      const int l = int(v & 0xFFFFu);
+      const uint32_t wp = (wcnt[l >> 1] >> (uint32_t(l & 1) * 16u)) & 0xFFFFu;
+      a.inv[size_t(wr0) * K + x] = gbase_s[l] + lbase_s[l] + int(wp) + int(v >> 16);
+    }
+  }
   grid_exit(pw.bar, grid);
 }
 

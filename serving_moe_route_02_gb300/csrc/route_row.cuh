@@ -32,6 +32,7 @@ struct RouteArgs {
   int32_t* offsets;       // [NE + 1]
   int32_t* perm;          // [T * k]
   int32_t* ids;           // [T, k] or nullptr
+  int32_t* inv = nullptr; // [T * k] or nullptr: position of entry t * k + j in perm
   int* err;               // device status word
   int T, k, Kg, off, cnt, NE;
   float scale;

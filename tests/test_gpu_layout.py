@@ -133,3 +133,38 @@ def test_layout_in_graph(mr):
     ref = oracle.route_layout(o["counts"], o["offsets"], o["perm"], 64, capacity=L["padded_rows"].numel())
     for key in ("inv_perm", "padded_offsets", "padded_rows", "m_indices"):
         assert np.array_equal(L[key].cpu().numpy(), ref[key]), key
+
+
+@pytest.mark.parametrize("cfg,path", [
+    (gen.cfg1(8), 0), (gen.cfg1(64, off=0, cnt=0), 0),           # decode kernel
+    (gen.cfg3(3000), 0), (gen.cfg3(3001, off=784, cnt=112), 0),  # approximate-score kernel
+    (gen.cfg3(3000, off=336, cnt=112), 3),                        # exact-score kernel
+    (gen.cfg4(T=2048, off=112, cnt=112), 0),                      # float32 logits (exact kernel)
+    (gen.cfg_decision_edges("plateau", 1500), 0),                 # slow extraction path
+], ids=["decode8_local", "decode64", "fast3000", "fast3001_local", "exact3000_local", "f32_2048",
+        "plateau"])
+def test_routing_writes_the_inverse(mr, cfg, path):
+    """moe_route_ex's inv_perm is the inverse of its perm and equals the oracle layout's
+    inverse of that perm; the other outputs equal moe_route's."""
+    dev = torch.device("cuda")
+    lg = torch.from_numpy(np.ascontiguousarray(cfg["logits"]).view(
+        np.int16 if cfg["dtype"] == "bf16" else np.float32)).to(dev)
+    if cfg["dtype"] == "bf16":
+        lg = lg.view(torch.bfloat16)
+    bias = torch.from_numpy(cfg["bias"]).to(dev)
+    prev = mr.set_path(path)
+    try:
+        ex = mr.route(lg, bias, local_offset=cfg["off"], local_count=cfg["cnt"], want_inv=True,
+                      want_ids=True)
+        plain = mr.route(lg, bias, local_offset=cfg["off"], local_count=cfg["cnt"], want_ids=True)
+    finally:
+        mr.set_path(prev)
+    torch.cuda.synchronize()
+    assert mr.device_status() == 0
+    for key in ("packed", "counts", "offsets", "perm", "ids"):
+        assert torch.equal(ex[key], plain[key]), key
+    perm = ex["perm"].cpu().numpy()
+    inv = ex["inv_perm"].cpu().numpy()
+    assert np.array_equal(perm[inv], np.arange(perm.size, dtype=np.int32))
+    ref = oracle.route_layout(ex["counts"].cpu().numpy(), ex["offsets"].cpu().numpy(), perm, tile=1)
+    assert np.array_equal(inv, ref["inv_perm"])
