@@ -129,7 +129,7 @@ int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T,
  *   sign kept (code bit 3); x_q holds two codes per byte, the even element in the low
  *   nibble.
  *   x         [T, H] bf16 bits, 16-byte aligned, finite; H % 32 == 0.
- *   x_q       [T, H / 2] bytes out, 2-byte aligned; x_scales [T, H / 32] bytes out.
+ *   x_q       [T, H / 2] bytes out, 4-byte aligned; x_scales [T, H / 32] bytes out.
  *   Routing arguments and outputs are those of moe_route (same results).
  * Errors: those of moe_route; INVALID_ARG for H <= 0, H % 32 != 0, NULL x / x_q /
  * x_scales with T > 0, or misaligned x / x_q; UNSUPPORTED for T > 64.  One kernel launch

@@ -240,7 +240,7 @@ int moe_route_quant(const void* logits, int logits_dtype, const float* bias, int
   if (T > 0 && (!logits || !packed || !perm || !x || !x_q || !x_scales)) return MOE_ROUTE_E_INVALID_ARG;
   if (H <= 0 || H % 32 != 0) return MOE_ROUTE_E_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(logits) % 16 != 0 || reinterpret_cast<uintptr_t>(bias) % 16 != 0 ||
-      reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(x_q) % 2 != 0)
+      reinterpret_cast<uintptr_t>(x) % 16 != 0 || reinterpret_cast<uintptr_t>(x_q) % 4 != 0)
     return MOE_ROUTE_E_INVALID_ARG;
   if (T > MOE_ROUTE_QUANT_MAX_TOKENS) return MOE_ROUTE_E_UNSUPPORTED;
   if (static_cast<long long>(T) * H >= (1ll << 31)) return MOE_ROUTE_E_UNSUPPORTED;

@@ -110,43 +110,56 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
   return r;
 }
 
-// Quantises blocks gw * 4 + 4 i * GW + (0..3) of the batch (warp gw of GW): lanes 8j..8j+7
-// take block j of a group of four, four elements each.
+// Quantises the batch's 32-element blocks (rows are contiguous, so block b starts at
+// element 32 b): warp gw of GW takes warp steps gw, gw + GW, ... of 8 blocks each, lanes
+// 4j..4j+3 block j of the step, 8 elements (16 bytes) per lane.  kQSteps steps' loads are
+// issued before any is converted, so a warp keeps 8 KB in flight.
+constexpr int kQSteps = 16;
 __device__ __forceinline__ void mxfp4_quant_blocks(const RouteArgs& a, int gw, int GW) {
   constexpr unsigned FULL = 0xffffffffu;
   const int lane = threadIdx.x & 31;
-  const int nbr = a.qH >> 5;  // blocks per row
-  const int nblk = a.T * nbr;
-  const int sub = lane & 7;
-  for (int b0 = gw * 4; b0 < nblk; b0 += GW * 4) {
-    const int b = b0 + (lane >> 3);
-    const bool act = b < nblk;
-    const int t = act ? b / nbr : 0;
-    const int c = act ? b - t * nbr : 0;
-    uint2 v = make_uint2(0u, 0u);
-    if (act) v = __ldg(reinterpret_cast<const uint2*>(a.qx + size_t(t) * a.qH + c * 32 + sub * 4));
-    // the block's largest magnitude, as bf16 magnitude bits (they order like the values)
-    uint32_t m = max(max(v.x & 0x7FFFu, (v.x >> 16) & 0x7FFFu), max(v.y & 0x7FFFu, (v.y >> 16) & 0x7FFFu));
-    m = max(m, __shfl_xor_sync(FULL, m, 1));
-    m = max(m, __shfl_xor_sync(FULL, m, 2));
-    m = max(m, __shfl_xor_sync(FULL, m, 4));
-    int e = -127;
-    if (m != 0u) {
-      // floor(log2 amax): the exponent field, or for a subnormal the leading mantissa bit
-      const int ex = int(m >> 7);
-      const int fl = ex > 0 ? ex - 127 : -133 + (31 - __clz(int(m)));
-      e = min(max(fl - 2, -127), 127);
+  const int sub = lane & 3;
+  const int nblk = a.T * (a.qH >> 5);
+  const int nstep = (nblk + 7) >> 3;
+  const uint4* xv = reinterpret_cast<const uint4*>(a.qx);
+  uint32_t* qv = reinterpret_cast<uint32_t*>(a.qcodes);
+  for (int s0 = gw; s0 < nstep; s0 += GW * kQSteps) {
+    uint4 v[kQSteps];
+#pragma unroll
+    for (int u = 0; u < kQSteps; ++u) {
+      const int b = (s0 + u * GW) * 8 + (lane >> 2);
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (b < nblk) v[u] = __ldg(xv + size_t(b) * 4 + sub);
     }
-    const float inv = __int_as_float(uint32_t(127 - e) << 23);  // 2^-e (e <= 125 for bf16)
-    const float f0 = __fmul_rn(__uint_as_float(v.x << 16), inv);
-    const float f1 = __fmul_rn(__uint_as_float(v.x & 0xFFFF0000u), inv);
-    const float f2 = __fmul_rn(__uint_as_float(v.y << 16), inv);
-    const float f3 = __fmul_rn(__uint_as_float(v.y & 0xFFFF0000u), inv);
-    const uint32_t bytes = e2m1x2(f0, f1) | (e2m1x2(f2, f3) << 8);
-    if (act) {
-      *reinterpret_cast<uint16_t*>(a.qcodes + size_t(t) * (a.qH >> 1) + c * 16 + sub * 2) =
-          static_cast<uint16_t>(bytes);
-      if (sub == 0) a.qscales[size_t(t) * nbr + c] = static_cast<uint8_t>(e + 127);
+#pragma unroll
+    for (int u = 0; u < kQSteps; ++u) {
+      const int b = (s0 + u * GW) * 8 + (lane >> 2);
+      // the block's largest magnitude, as bf16 magnitude bits (they order like the values)
+      const uint32_t mm = __vmaxu2(__vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
+                                   __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu));
+      uint32_t m = max(mm & 0xFFFFu, mm >> 16);
+      m = max(m, __shfl_xor_sync(FULL, m, 1));
+      m = max(m, __shfl_xor_sync(FULL, m, 2));
+      int e = -127;
+      if (m != 0u) {
+        // floor(log2 amax): the exponent field, or for a subnormal the leading mantissa bit
+        const int ex = int(m >> 7);
+        const int fl = ex > 0 ? ex - 127 : -133 + (31 - __clz(int(m)));
+        e = min(max(fl - 2, -127), 127);
+      }
+      const float inv = __int_as_float(uint32_t(127 - e) << 23);  // 2^-e (e <= 125 for bf16)
+      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+      uint32_t word = 0u;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = __fmul_rn(__uint_as_float(w4[i] << 16), inv);
+        const float hi = __fmul_rn(__uint_as_float(w4[i] & 0xFFFF0000u), inv);
+        word |= e2m1x2(lo, hi) << (8 * i);
+      }
+      if (b < nblk) {
+        qv[size_t(b) * 4 + sub] = word;
+        if (sub == 0) a.qscales[b] = static_cast<uint8_t>(e + 127);
+      }
     }
   }
 }
@@ -206,9 +219,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
              uint32_t(nrows) * L::ROWB, mbar);
   }
-  // the activations' quantisation overlaps the row copies in flight
-  if constexpr (QUANT) mxfp4_quant_blocks(a, crank * kDecodeRowsPerCta + w, nctas * kDecodeRowsPerCta);
-  if (have) mbar_wait_bounded(mbar, 0, a.err);
+  // the activations' quantisation: by the warps that route no row (warps rpc.. of every
+  // CTA), while the others route; by all warps, ahead of the row wait, if none is free
+  bool quant_warp = false;
+  if constexpr (QUANT) {
+    const int qw = kDecodeRowsPerCta - rpc;
+    quant_warp = qw > 0 && w >= rpc;
+    if (qw <= 0) mxfp4_quant_blocks(a, crank * kDecodeRowsPerCta + w, nctas * kDecodeRowsPerCta);
+    else if (quant_warp) mxfp4_quant_blocks(a, crank * qw + (w - rpc), nctas * qw);
+  }
+  if (have && !quant_warp) mbar_wait_bounded(mbar, 0, a.err);
 
   SlotOut o = {};
   if constexpr (DT == DT_PACKED) {

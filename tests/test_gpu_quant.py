@@ -93,6 +93,7 @@ def test_route_quant_empty_and_errors(mr):
     assert call(H=0) == mr.E_INVALID_ARG
     assert call(xp=ctypes.c_void_p(x.data_ptr() + 2)) == mr.E_INVALID_ARG
     assert call(qp=ctypes.c_void_p(xq.data_ptr() + 1)) == mr.E_INVALID_ARG
+    assert call(qp=ctypes.c_void_p(xq.data_ptr() + 2)) == mr.E_INVALID_ARG
     out["counts"].fill_(-1)
     assert call(T=0) == mr.OK
     torch.cuda.synchronize()
