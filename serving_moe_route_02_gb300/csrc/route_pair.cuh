@@ -62,6 +62,26 @@ __device__ __forceinline__ float fsub_down(float a, float b) {
 constexpr int kPairEPL = 56;   // experts per lane
 constexpr int kChain = 28;     // experts per chain
 
+// c'' in shared memory: per lane, the pairs (chain a, chain b) of its 28 words, 60 floats
+// apart (56 used), so that 8 lanes' 16-byte loads fall on distinct banks
+constexpr int kCppStride = 60;
+constexpr int kCppFloats = 16 * kCppStride;
+
+// One packed approximate score word: b'' for x = (xa, xb) and c'' = (ca, cb), f16 pair
+// (xa's low).  The halving and the fma run on f32 pairs (mul.rn.f32x2, fma.rn.f32x2),
+// which round like their scalar forms, so each half equals
+// f16(fma(0.5, tanh.approx(x * 0.5), c)).
+__device__ __forceinline__ uint32_t approx_word(float xa, float xb, uint64_t c2) {
+  uint32_t v;
+  asm("{\n\t.reg .b64 x, q, t, r;\n\t.reg .b32 t0, t1, r0, r1;\n\t"
+      "mov.b64 x, {%1, %2};\n\tmul.rn.f32x2 q, x, %4;\n\tmov.b64 {t0, t1}, q;\n\t"
+      "tanh.approx.f32 t0, t0;\n\ttanh.approx.f32 t1, t1;\n\tmov.b64 t, {t0, t1};\n\t"
+      "fma.rn.f32x2 r, t, %4, %3;\n\tmov.b64 {r0, r1}, r;\n\tcvt.rn.f16x2.f32 %0, r1, r0;\n\t}"
+      : "=r"(v)
+      : "f"(xa), "f"(xb), "l"(c2), "l"(0x3F0000003F000000ull));
+  return v;
+}
+
 // Per-warp shared scratch of route_pair.
 struct PairScratch {
   uint32_t pool[2][16];   // per row: the 32 kept chains' top-2 values, f16 pairs
@@ -228,23 +248,19 @@ __device__ __forceinline__ SlotOut route_pair(const void* row0, const void* row1
   {
     const uint2* pa = reinterpret_cast<const uint2*>(row + e0);
     const uint2* pb = reinterpret_cast<const uint2*>(row + e0 + kChain);
-    const float4* ca = reinterpret_cast<const float4*>(cpp_s + e0);
-    const float4* cb = reinterpret_cast<const float4*>(cpp_s + e0 + kChain);
+    const ulonglong2* cq = reinterpret_cast<const ulonglong2*>(cpp_s + h * kCppStride);
 #pragma unroll
     for (int q = 0; q < kChain / 4; ++q) {
       const uint2 va = pa[q], vb = pb[q];
-      const float4 cva = ca[q], cvb = cb[q];
+      const ulonglong2 c01 = cq[2 * q], c23 = cq[2 * q + 1];
       const float xa[4] = {__uint_as_float(va.x << 16), __uint_as_float(va.x & 0xFFFF0000u),
                            __uint_as_float(va.y << 16), __uint_as_float(va.y & 0xFFFF0000u)};
       const float xb[4] = {__uint_as_float(vb.x << 16), __uint_as_float(vb.x & 0xFFFF0000u),
                            __uint_as_float(vb.y << 16), __uint_as_float(vb.y & 0xFFFF0000u)};
-      const float cax[4] = {cva.x, cva.y, cva.z, cva.w};
-      const float cbx[4] = {cvb.x, cvb.y, cvb.z, cvb.w};
+      const uint64_t cc[4] = {c01.x, c01.y, c23.x, c23.y};
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float fa = __fmaf_rn(0.5f, tanh_approx(__fmul_rn(xa[r], 0.5f)), cax[r]);
-        const float fb = __fmaf_rn(0.5f, tanh_approx(__fmul_rn(xb[r], 0.5f)), cbx[r]);
-        const uint32_t v = h2pack(fa, fb);
+        const uint32_t v = approx_word(xa[r], xb[r], cc[r]);
         bp[4 * q + r] = v;
         if (r & 1) {
           const uint32_t t = h2min(m1o, v);

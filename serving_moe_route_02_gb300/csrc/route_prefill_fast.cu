@@ -40,8 +40,8 @@ struct FastSmem {
   static constexpr int SLOTB = 2 * ROWB;           // a pair of rows
   static constexpr int WORDS = kMaxBins / 2;       // 16-bit counters, two per word
   static constexpr int o_bias = 0;
-  static constexpr int o_cpp = f_align(o_bias + kE * 4, 128);   // c'' = bias + 0.5 - o
-  static constexpr int o_ring = f_align(o_cpp + kE * 4, 128);
+  static constexpr int o_cpp = f_align(o_bias + kE * 4, 128);   // c'' = bias + 0.5 - o, in pairs
+  static constexpr int o_ring = f_align(o_cpp + kCppFloats * 4, 128);
   static constexpr int o_wcnt = o_ring + NW * D * SLOTB;
   static constexpr int o_ws = f_align(o_wcnt + NW * WORDS * 4, 128);
   static constexpr int o_hist = f_align(o_ws + NW * int(sizeof(PairScratch)), 128);
@@ -156,7 +156,13 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     }
     pbnd = pair_bounds(a.eps_half, fkey_inv(bmn), fkey_inv(bmx));
   }
-  for (int e = tid; e < kE; e += NT) cpp_s[e] = __fadd_rn(bias_s[e], pbnd.d0);
+  // c'' in the pair order route_pair reads: lane h's word j pairs expert 56 h + j with
+  // expert 56 h + 28 + j
+  for (int e = tid; e < kE; e += NT) {
+    const int hh = e / kPairEPL, r = e - hh * kPairEPL;
+    const int c = r >= kChain ? 1 : 0, j = r - c * kChain;
+    cpp_s[hh * kCppStride + 2 * j + c] = __fadd_rn(bias_s[e], pbnd.d0);
+  }
   __syncthreads();
 
   // ---- phase 1: route this warp's rows two at a time, rank their entries within the warp
