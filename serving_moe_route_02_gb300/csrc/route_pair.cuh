@@ -226,6 +226,22 @@ __device__ __forceinline__ float half_minf(float v) {
   return v;
 }
 
+// Bits of the words of a lane whose values reach `thr2` (an f16 pair holding the same
+// threshold twice): bit q of *ma for element q of chain a, of *mb for chain b.
+__device__ __forceinline__ void chain_masks(const uint32_t (&bp)[kChain], uint32_t thr2, uint32_t& ma,
+                                            uint32_t& mb) {
+  uint32_t acc0 = 0, acc1 = 0;
+#pragma unroll
+  for (int q = 0; q < kChain; ++q) {
+    const uint32_t pat = (1u << (q % 14)) * 0x10001u;
+    const uint32_t t = h2ge(bp[q], thr2) & pat;
+    if (q < 14) acc0 |= t;
+    else acc1 |= t;
+  }
+  ma = (acc0 & 0x3FFFu) | ((acc1 & 0x3FFFu) << 14);
+  mb = (acc0 >> 16) | ((acc1 >> 16) << 14);
+}
+
 // Routes two bf16 rows: `row0` for lanes 0-15, `row1` for lanes 16-31 (shared memory,
 // 16-byte aligned; both may be the same row).  `bias_s`: biases; `cpp_s`: c'' = bias + d0
 // (shared memory); `stab`: the exact score table (global memory, read-only).  All 32 lanes call it;
@@ -279,14 +295,16 @@ __device__ __forceinline__ SlotOut route_pair(const void* row0, const void* row1
   const uint32_t m2 = h2max(h2min(m1e, m1o), h2max(m2e, m2o));
 
   // ---- approximate group scores (f32): lane top-2 over both chains, then the partner lane
-  float gs;
+  float gs, g2;
   {
     const float a1 = h_lo(m1), a2 = h_lo(m2), b1 = h_hi(m1), b2 = h_hi(m2);
     float l1 = fmaxf(a1, b1), l2 = fmax3(fminf(a1, b1), a2, b2);
     const float p1 = __shfl_xor_sync(FULL, l1, 1), p2 = __shfl_xor_sync(FULL, l2, 1);
-    const float g2 = fmax3(fminf(l1, p1), l2, p2);
+    g2 = fmax3(fminf(l1, p1), l2, p2);
     gs = __fadd_rn(fmaxf(l1, p1), g2);
   }
+  // exact biased score of an expert of this half's row
+  auto exact_b = [&](int id) -> float { return __fadd_rn(__ldg(stab + sig_index(row[id])), bias_s[id]); };
 
   // ---- kept groups per half: rank among the 8 (ties to the lower group); certain when
   //      min(kept) - max(dropped) > 2 delta
@@ -303,24 +321,37 @@ __device__ __forceinline__ SlotOut route_pair(const void* row0, const void* row1
     const float nmax = half_maxf(kept ? -INFINITY : gs);
     const bool certain = pb.ok && __fsub_rn(kmin, nmax) > 2.0f * pb.delta;
     if (!__all_sync(FULL, certain)) {
-      // exact group scores from the table for both rows
-      const float* tab_lo = stab - kSigLo;
-      float y1 = -INFINITY, y2 = -INFINITY, z1 = -INFINITY, z2 = -INFINITY;
-      const uint2* p = reinterpret_cast<const uint2*>(row + e0);
-      const float4* bq = reinterpret_cast<const float4*>(bias_s + e0);
-#pragma unroll 2
-      for (int q = 0; q < kPairEPL / 4; ++q) {
-        const uint2 v = p[q];
-        const float4 bb = bq[q];
-        float s0, s1, s2, s3;
-        sig_bf16_pair(tab_lo, v.x, s0, s1);
-        sig_bf16_pair(tab_lo, v.y, s2, s3);
-        top2_pair(y1, y2, __fadd_rn(s0, bb.x), __fadd_rn(s1, bb.y));
-        top2_pair(z1, z2, __fadd_rn(s2, bb.z), __fadd_rn(s3, bb.w));
-      }
-      float l1 = fmaxf(y1, z1), l2 = fmax3(fminf(y1, z1), y2, z2);
-      const float p1 = __shfl_xor_sync(FULL, l1, 1), p2 = __shfl_xor_sync(FULL, l2, 1);
-      const float egs = __fadd_rn(fmaxf(l1, p1), fmax3(fminf(l1, p1), l2, p2));
+      // exact group scores for both rows.  Two experts of the group have b'' >= g2 (its
+      // approximate second largest), so its exact second largest is at least g2 + o - eps,
+      // and an expert among its exact top-2 has b'' >= g2 - 2 eps: only those
+      // ("candidates", one or two per lane as a rule) are looked up, four at a time.
+      uint32_t ra, rb;
+      chain_masks(bp, pb.ok ? h2dup_down(fsub_down(g2, 2.0f * pb.eps)) : 0xFC00FC00u, ra, rb);
+      float y1 = -INFINITY, y2 = -INFINITY;
+      do {
+        int id[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          id[i] = -1;
+          if (ra) {
+            id[i] = e0 + __ffs(ra) - 1;
+            ra &= ra - 1u;
+          } else if (rb) {
+            id[i] = e0 + kChain + __ffs(rb) - 1;
+            rb &= rb - 1u;
+          }
+        }
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = id[i] >= 0 ? exact_b(id[i]) : -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          y2 = fmaxf(y2, fminf(y1, v[i]));
+          y1 = fmaxf(y1, v[i]);
+        }
+      } while (ra | rb);
+      const float p1 = __shfl_xor_sync(FULL, y1, 1), p2 = __shfl_xor_sync(FULL, y2, 1);
+      const float egs = __fadd_rn(fmaxf(y1, p1), fmax3(fminf(y1, p1), y2, p2));
       int er = 0;
 #pragma unroll
       for (int g = 0; g < kG; ++g) {
@@ -347,19 +378,9 @@ __device__ __forceinline__ SlotOut route_pair(const void* row0, const void* row1
   const uint32_t cut2 = pb.ok ? h2dup_down(cutf) : 0xFC00FC00u;
 
   // ---- survivors: a bit per kept expert with b'' >= cut (chain a: bits of ma, b: mb)
-  uint32_t acc0 = 0, acc1 = 0;
-#pragma unroll
-  for (int q = 0; q < kChain; ++q) {
-    const uint32_t pat = (1u << (q % 14)) * 0x10001u;
-    const uint32_t t = h2ge(bp[q], cut2) & pat;
-    if (q < 14) acc0 |= t;
-    else acc1 |= t;
-  }
-  uint32_t ma = 0, mb = 0;
-  if (kept) {
-    ma = (acc0 & 0x3FFFu) | ((acc1 & 0x3FFFu) << 14);
-    mb = (acc0 >> 16) | ((acc1 >> 16) << 14);
-  }
+  uint32_t ma, mb;
+  chain_masks(bp, cut2, ma, mb);
+  if (!kept) ma = mb = 0u;
   const int cnt = __popc(ma) + __popc(mb);
   int incl = cnt;
 #pragma unroll
