@@ -1,6 +1,6 @@
 // route_prefill_fast.cu -- prefill-size routing of bf16 logits for the Kimi-K3 instance
 // (E = 896 in 8 groups, k = 16, keep 4 groups) in one persistent, cooperative launch:
-// one CTA of 16 warps per SM, a contiguous row range per CTA and per warp.  The exact
+// one CTA of 20 warps per SM, a contiguous row range per CTA and per warp.  The exact
 // score table stays in global memory (read through the L1 cache): only the survivors of
 // each row, about 18 of 896, and the rare exact group scores look it up.
 //
@@ -33,27 +33,31 @@ namespace {
 
 __host__ __device__ constexpr int f_align(int x, int a) { return (x + a - 1) / a * a; }
 
+// Bins of the instance this kernel serves: 896 global ids, or at most 896 rank-local ids
+// plus 16 for the other ranks' slots, rounded up to a multiple of 4.
+constexpr int kFastBins = kE + 16;
+
 struct FastSmem {
-  static constexpr int NW = 16;                    // warps per CTA
+  static constexpr int NW = 20;                    // warps per CTA
   static constexpr int D = 2;                      // pairs of rows in flight per warp
   static constexpr int ROWB = kE * 2;              // one bf16 row: 1,792 bytes
   static constexpr int SLOTB = 2 * ROWB;           // a pair of rows
-  static constexpr int WORDS = kMaxBins / 2;       // 16-bit counters, two per word
+  static constexpr int WORDS = kFastBins / 2;      // 16-bit counters, two per word
   static constexpr int o_bias = 0;
   static constexpr int o_cpp = f_align(o_bias + kE * 4, 128);   // c'' = bias + 0.5 - o, in pairs
   static constexpr int o_ring = f_align(o_cpp + kCppFloats * 4, 128);
   static constexpr int o_wcnt = o_ring + NW * D * SLOTB;
   static constexpr int o_ws = f_align(o_wcnt + NW * WORDS * 4, 128);
   static constexpr int o_hist = f_align(o_ws + NW * int(sizeof(PairScratch)), 128);
-  static constexpr int o_lbase = f_align(o_hist + (kMaxBins + 1) * 4, 128);
-  static constexpr int o_gbase = f_align(o_lbase + (kMaxBins + 1) * 4, 128);
-  static constexpr int o_tmp = f_align(o_gbase + (kMaxBins + 1) * 4, 128);
+  static constexpr int o_lbase = f_align(o_hist + (kFastBins + 1) * 4, 128);
+  static constexpr int o_gbase = f_align(o_lbase + (kFastBins + 1) * 4, 128);
+  static constexpr int o_tmp = f_align(o_gbase + (kFastBins + 1) * 4, 128);
   static constexpr int o_mbar = f_align(o_tmp + 64 * 4, 128);
   static constexpr int o_ent = f_align(o_mbar + (NW * D + 1) * 8, 128);
-  // (id, rank) of each entry, per warp, in the room left
-  static constexpr int ENT_PER_WARP = (227 * 1024 - o_ent) / (NW * 4) / 32 * 32;
+  // (id, rank) of each entry, 16 bits (id | rank << 10), per warp, in the room left
+  static constexpr int ENT_PER_WARP = (227 * 1024 - o_ent) / (NW * 2) / 32 * 32;
   static constexpr int ROWS_PER_WARP = ENT_PER_WARP / 16;
-  static constexpr int total = o_ent + NW * ENT_PER_WARP * 4;
+  static constexpr int total = o_ent + NW * ENT_PER_WARP * 2;
   // the CTA's sorted entries, in the ring once phase 1 is over: values, then bins
   static constexpr int SORT_CAP = (NW * D * SLOTB) / 6 / 8 * 8;
   static constexpr int o_sval = o_ring;
@@ -62,7 +66,10 @@ struct FastSmem {
 
 static_assert(FastSmem::total <= 227 * 1024, "fast prefill smem exceeds 227 KB");
 static_assert(FastSmem::SORT_CAP >= FastSmem::NW * FastSmem::ENT_PER_WARP, "sorted entries fit the ring");
-static_assert(FastSmem::ROWS_PER_WARP >= 32, "room for the entries of 32 rows per warp");
+static_assert(FastSmem::ROWS_PER_WARP >= 22, "room for 65,536 rows on 152 SMs");
+static_assert(FastSmem::ROWS_PER_WARP <= 64, "a rank within a warp fits 6 bits");
+static_assert(kFastBins <= 1024, "an id fits 10 bits");
+static_assert(2 * FastSmem::NW + 2 <= 64, "the bias range reduction and the barrier flag fit tmp");
 static_assert(FastSmem::ROWB % 128 == 0, "row slots keep 128-byte alignment");
 
 }  // namespace
@@ -102,7 +109,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   uint8_t* ring = ring_all + w * L::D * L::SLOTB;
   uint64_t* mb = mbar_all + w * L::D;
   uint32_t* wcnt = wcnt_all + w * L::WORDS;
-  uint32_t* ent = reinterpret_cast<uint32_t*>(smem + L::o_ent) + w * L::ENT_PER_WARP;
+  uint16_t* ent = reinterpret_cast<uint16_t*>(smem + L::o_ent) + w * L::ENT_PER_WARP;
   const uint8_t* logits = static_cast<const uint8_t*>(a.logits);
   const int nwords = a.NE / 2;  // NE is a multiple of 4
 
@@ -145,14 +152,14 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     const uint32_t kmn = __reduce_min_sync(0xffffffffu, fkey(mn));
     if (lane == 0) {
       tmp[w] = int(kmx);
-      tmp[16 + w] = int(kmn);
+      tmp[NW + w] = int(kmn);
     }
     __syncthreads();
     uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
 #pragma unroll
     for (int i = 0; i < NW; ++i) {
       bmx = max(bmx, uint32_t(tmp[i]));
-      bmn = min(bmn, uint32_t(tmp[16 + i]));
+      bmn = min(bmn, uint32_t(tmp[NW + i]));
     }
     pbnd = pair_bounds(a.eps_half, fkey_inv(bmn), fkey_inv(bmx));
   }
@@ -188,12 +195,12 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     const uint32_t sh = uint32_t(o.lid & 1) * 16u;
     if (half == 0) {
       const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
-      ent[i * K + h] = uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 16);
+      ent[i * K + h] = static_cast<uint16_t>(uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 10));
     }
     __syncwarp();
     if (half == 1 && valid) {
       const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
-      ent[i * K + h] = uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 16);
+      ent[i * K + h] = static_cast<uint16_t>(uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 10));
     }
     __syncwarp();
     if (lane == 0 && p + L::D < npairs) {
@@ -230,9 +237,9 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   const int nrouted = fail_at < 0 ? nw : 2 * fail_at;
   for (int x = lane; x < nrouted * K; x += 32) {
     const uint32_t v = ent[x];
-    const int l = int(v & 0xFFFFu);
+    const int l = int(v & 0x3FFu);
     const uint32_t wp = (wcnt[l >> 1] >> (uint32_t(l & 1) * 16u)) & 0xFFFFu;
-    const int lp = lbase_s[l] + int(wp) + int(v >> 16);
+    const int lp = lbase_s[l] + int(wp) + int(v >> 10);
     sval[lp] = (wr0 + x / K) * K + (x % K);
     sbin[lp] = static_cast<uint16_t>(l);
   }
@@ -273,9 +280,9 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     // the warp give its CTA-local position, gbase the rest
     for (int x = lane; x < nrouted * K; x += 32) {
       const uint32_t v = ent[x];
-      const int l = int(v & 0xFFFFu);
+      const int l = int(v & 0x3FFu);
       const uint32_t wp = (wcnt[l >> 1] >> (uint32_t(l & 1) * 16u)) & 0xFFFFu;
-      a.inv[size_t(wr0) * K + x] = gbase_s[l] + lbase_s[l] + int(wp) + int(v >> 16);
+      a.inv[size_t(wr0) * K + x] = gbase_s[l] + lbase_s[l] + int(wp) + int(v >> 10);
     }
   }
   grid_exit(pw.bar, grid);
@@ -298,7 +305,8 @@ bool prefill_fast_fits(int T, int grid) {
 
 cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, int grid,
                                       cudaStream_t st) {
-  if (!prefill_fast_fits(a.T, grid) || a.k != 16 || a.Kg != 4) return cudaErrorInvalidValue;
+  if (!prefill_fast_fits(a.T, grid) || a.k != 16 || a.Kg != 4 || a.NE > kFastBins)
+    return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(FastSmem::NW * 32, 1, 1);
