@@ -407,29 +407,24 @@ __device__ __forceinline__ SlotOut route_pair(const void* row0, const void* row1
     for (uint32_t m = ma; m; m &= m - 1u) ws.sid[half][pos++] = e0 + __ffs(m) - 1;
     for (uint32_t m = mb; m; m &= m - 1u) ws.sid[half][pos++] = e0 + kChain + __ffs(m) - 1;
     __syncwarp();
-    // survivors 2h and 2h + 1 of this half
+    // survivors 2h and 2h + 1 of this half (total >= 16, so both indices below exist;
+    // the lookups of lanes past the total are discarded)
+    const bool v0 = 2 * h < total, v1 = 2 * h + 1 < total;
     uint32_t k0 = 0, k1 = 0;
-    float bx0 = 0.0f, bx1 = 0.0f;
-    if (2 * h < total) {
-      float s;
-      bx0 = exact(ws.sid[half][2 * h], &s);
-      ws.ss[half][2 * h] = s;
-    }
-    if (2 * h + 1 < total) {
-      float s;
-      bx1 = exact(ws.sid[half][2 * h + 1], &s);
-      ws.ss[half][2 * h + 1] = s;
-    }
+    float s0, s1;
+    const float bx0 = exact(ws.sid[half][min(2 * h, total - 1)], &s0);
+    const float bx1 = exact(ws.sid[half][min(2 * h + 1, total - 1)], &s1);
+    if (v0) ws.ss[half][2 * h] = s0;
+    if (v1) ws.ss[half][2 * h + 1] = s1;
     __syncwarp();  // the survivors' exact scores are read by the slot owners below
-    bool keys32 = base > 0.0f;
+    // keys of 32 bits: every survivor's exact b is at least base, so they fit when base is
+    // positive and each lies less than 2^26 float steps above it
+    const uint32_t bb = __float_as_uint(base);
+    const bool keys32 = base > 0.0f && (!v0 || __float_as_uint(bx0) - bb < (1u << 26)) &&
+                        (!v1 || __float_as_uint(bx1) - bb < (1u << 26));
     if (__all_sync(FULL, keys32)) {
-      const uint32_t bm = half_max(max(2 * h < total ? __float_as_uint(bx0) : 0u,
-                                       2 * h + 1 < total ? __float_as_uint(bx1) : 0u));
-      keys32 = (bm - __float_as_uint(base)) < (1u << 26);
-    }
-    if (__all_sync(FULL, keys32)) {
-      if (2 * h < total) k0 = ((__float_as_uint(bx0) - __float_as_uint(base) + 1u) << 5) | uint32_t(31 - 2 * h);
-      if (2 * h + 1 < total) k1 = ((__float_as_uint(bx1) - __float_as_uint(base) + 1u) << 5) | uint32_t(30 - 2 * h);
+      if (v0) k0 = ((__float_as_uint(bx0) - bb + 1u) << 5) | uint32_t(31 - 2 * h);
+      if (v1) k1 = ((__float_as_uint(bx1) - bb + 1u) << 5) | uint32_t(30 - 2 * h);
       bitonic32_u32(k0, k1, h);
       // positions 0..15 (lanes 0..7 of the half) are slots 0..15
       if (h < 8) {

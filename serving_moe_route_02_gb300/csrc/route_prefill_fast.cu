@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   // every routed entry to its CTA-local sorted position (the ring is free now); after a
   // wait that ran out only the rows before it were routed and counted
   const int nrouted = fail_at < 0 ? nw : 2 * fail_at;
+#pragma unroll 4
   for (int x = lane; x < nrouted * K; x += 32) {
     const uint32_t v = ent[x];
     const int l = int(v & 0x3FFu);
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   for (int e = tid; e < a.NE; e += NT) gbase_s[e] += off_s[e] - lbase_s[e];
   __syncthreads();
   const int nvalid = lbase_s[a.NE];
+#pragma unroll 4
   for (int i = tid; i < nvalid; i += NT) a.perm[gbase_s[sbin[i]] + i] = sval[i];
   if (a.inv) {
     // each entry's place in perm, in token order (coalesced): warp prefix + rank within
