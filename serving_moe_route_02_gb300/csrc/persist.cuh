@@ -42,6 +42,47 @@ __device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned nblocks, in
   return *flag_s != 0;
 }
 
+// The same barrier in two halves, so that a CTA can do work of its own between arriving
+// and waiting.  grid_arrive: every thread calls it once the writes to publish are done;
+// thread 0 returns the counter's value before its arrival (the others 0), which
+// grid_wait needs.  CTA `skip_cta` does not arrive (the timeout test).
+__device__ __forceinline__ unsigned grid_arrive(unsigned* bar, unsigned nblocks, int skip_cta = -1) {
+  __syncthreads();
+  unsigned old = 0u;
+  if (threadIdx.x == 0 && int(blockIdx.x) != skip_cta) {
+    const unsigned add = (blockIdx.x == 0) ? 0x80000000u - (nblocks - 1u) : 1u;
+    // release: the CTA's writes ordered before it by the block barrier above
+    asm volatile("atom.release.gpu.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(bar), "r"(add) : "memory");
+  }
+  return old;
+}
+// grid_wait: every thread calls it; true once every CTA has arrived, false if the wait ran
+// out (the status word then holds a timeout) or at once in CTA `skip_cta`.
+__device__ __forceinline__ bool grid_wait(unsigned* bar, unsigned old, int* err, int* flag_s,
+                                          uint64_t limit_ns = kWaitLimitNs, int skip_cta = -1) {
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    if (int(blockIdx.x) == skip_cta) {
+      ok = 0;
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        unsigned cur;
+        asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(cur) : "l"(bar) : "memory");
+        if ((cur ^ old) & 0x80000000u) break;
+        if (globaltimer_ns() - t0 > limit_ns) {
+          atomicExch(err, kErrTimeout);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    *flag_s = ok;
+  }
+  __syncthreads();
+  return *flag_s != 0;
+}
+
 // Every CTA calls this once on its way out, on every path (also after a wait that ran
 // out).  The last CTA to leave puts the barrier words back to zero, so a call that gave
 // up mid-barrier does not leave the next call a half-counted barrier.  bar[1] counts
@@ -82,8 +123,8 @@ __device__ __forceinline__ void block_scan_fast(const int* in, int* out, int n, 
   }
   if (lane == 31) tmp[wid] = incl;
   __syncthreads();
-  int run = incl - sum;
-  for (int i = 0; i < wid; ++i) run += tmp[i];
+  // the warps before this one, summed in one warp reduction (at most 32 warps)
+  int run = incl - sum + int(__reduce_add_sync(0xffffffffu, unsigned(lane < wid ? tmp[lane] : 0)));
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if (lo + i < hi) {

@@ -13,11 +13,12 @@
 //   the same id, in (token, slot) order, since a warp routes its rows in order and ids
 //   are unique in a row.  (id, rank) is kept in shared memory.
 // CTA tail of phase 1: a column pass over the warps' counters gives each warp's prefix
-//   per id and the CTA's histogram, which goes to the expert-major matrix hist[bin][cta];
-//   a block scan gives the CTA-local bin offsets, and every entry is placed at its
-//   CTA-local position (bin offset + warp prefix + rank) in a buffer that replaces the
-//   ring: the CTA's entries sorted by (id, token, slot).
-// Grid barrier 1, column scan over CTAs (prefixes and totals), grid barrier 2.
+//   per id and the CTA's histogram, which goes to the expert-major matrix hist[bin][cta].
+//   The CTA then arrives at grid barrier 1 and, before it waits, a block scan gives the
+//   CTA-local bin offsets and every entry is placed at its CTA-local position (bin
+//   offset + warp prefix + rank) in a buffer that replaces the ring: the CTA's entries
+//   sorted by (id, token, slot).
+// Grid barrier 1 (wait), column scan over CTAs (prefixes and totals), grid barrier 2.
 // Phase 3: offsets from the totals (CTA 0 writes counts and offsets); the sorted buffer
 //   goes to perm in runs of consecutive addresses, one run per bin.
 // Every wait is bounded in time; a wait that runs out sets the status word and the CTA
@@ -231,6 +232,9 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   }
   __syncthreads();
   for (int e = tid; e < a.NE; e += NT) pw.hist[size_t(e) * pw.grid_max + cta] = hist_s[e];
+  // grid barrier 1, split: arrive once the histogram is out; the CTA-local work below
+  // overlaps the wait for the other CTAs
+  const unsigned arrival = grid_arrive(pw.bar, grid, a.barrier_skip_cta);
   block_scan_fast(hist_s, lbase_s, a.NE, tmp);
   // every routed entry to its CTA-local sorted position (the ring is free now); after a
   // wait that ran out only the rows before it were routed and counted
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   }
 
   int* flag_s = tmp + 32;
-  if (!grid_barrier(pw.bar, grid, a.err, flag_s, a.barrier_wait_ns, a.barrier_skip_cta)) {
+  if (!grid_wait(pw.bar, arrival, a.err, flag_s, a.barrier_wait_ns, a.barrier_skip_cta)) {
     grid_exit(pw.bar, grid);
     return;
   }
