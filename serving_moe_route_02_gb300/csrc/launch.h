@@ -12,7 +12,7 @@ struct PrefillWS {
   int* hist;       // [kMaxBins][grid_max] per-CTA histograms, expert-major
   int* prefix;     // [kMaxBins][grid_max] exclusive prefix over CTAs
   int* counts;     // [kMaxBins]
-  unsigned* bar;   // [2]: arrival count, generation
+  unsigned* bar;   // [2]: arrival counter, exit counter
   int grid_max;
 };
 

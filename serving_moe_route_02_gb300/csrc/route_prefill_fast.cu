@@ -18,7 +18,8 @@
 //   CTA-local bin offsets and every entry is placed at its CTA-local position (bin
 //   offset + warp prefix + rank) in a buffer that replaces the ring: the CTA's entries
 //   sorted by (id, token, slot).
-// Grid barrier 1 (wait), column scan over CTAs (prefixes and totals), grid barrier 2.
+// Grid barrier 1 (wait), column scan over CTAs (prefixes and totals), grid barrier 2 (the
+//   CTAs that own bins of the scan place their entries after it, before they wait).
 // Phase 3: offsets from the totals (CTA 0 writes counts and offsets); the sorted buffer
 //   goes to perm in runs of consecutive addresses, one run per bin.
 // Every wait is bounded in time; a wait that runs out sets the status word and the CTA
@@ -239,15 +240,21 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   // every routed entry to its CTA-local sorted position (the ring is free now); after a
   // wait that ran out only the rows before it were routed and counted
   const int nrouted = fail_at < 0 ? nw : 2 * fail_at;
+  auto place = [&]() {
 #pragma unroll 4
-  for (int x = lane; x < nrouted * K; x += 32) {
-    const uint32_t v = ent[x];
-    const int l = int(v & 0x3FFu);
-    const uint32_t wp = (wcnt[l >> 1] >> (uint32_t(l & 1) * 16u)) & 0xFFFFu;
-    const int lp = lbase_s[l] + int(wp) + int(v >> 10);
-    sval[lp] = (wr0 + x / K) * K + (x % K);
-    sbin[lp] = static_cast<uint16_t>(l);
-  }
+    for (int x = lane; x < nrouted * K; x += 32) {
+      const uint32_t v = ent[x];
+      const int l = int(v & 0x3FFu);
+      const uint32_t wp = (wcnt[l >> 1] >> (uint32_t(l & 1) * 16u)) & 0xFFFFu;
+      const int lp = lbase_s[l] + int(wp) + int(v >> 10);
+      sval[lp] = (wr0 + x / K) * K + (x % K);
+      sbin[lp] = static_cast<uint16_t>(l);
+    }
+  };
+  // the CTAs that own bins of the column scan place their entries after it, while they
+  // wait at grid barrier 2, so that the scan starts as soon as barrier 1 opens
+  const bool scanner = cta * NW < a.NE;
+  if (!scanner) place();
 
   int* flag_s = tmp + 32;
   if (!grid_wait(pw.bar, arrival, a.err, flag_s, a.barrier_wait_ns, a.barrier_skip_cta)) {
@@ -255,7 +262,9 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     return;
   }
   column_scan(pw, a.NE, grid, NW);
-  if (!grid_barrier(pw.bar, grid, a.err, flag_s, a.barrier_wait_ns)) {
+  const unsigned arrival2 = grid_arrive(pw.bar, grid);
+  if (scanner) place();
+  if (!grid_wait(pw.bar, arrival2, a.err, flag_s, a.barrier_wait_ns)) {
     grid_exit(pw.bar, grid);
     return;
   }
