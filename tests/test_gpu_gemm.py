@@ -76,3 +76,56 @@ def test_router_gemm_rejects(mr, weight):
     with pytest.raises(mr.MoeRouteError) as e:
         mr.router_gemm_route(hid, w_dev, bias)
     assert e.value.status == mr.E_UNSUPPORTED
+
+
+def test_router_gemm_repeated_and_replayed(mr, weight):
+    """Back-to-back calls chain the contraction and the routing as programmatic
+    dependents: outputs cleared before each call come back whole, over calls of two batch
+    shapes in turn on one stream and over replays of a captured graph of them."""
+    _, w_dev = weight
+    cases = []
+    for T, off, cnt in ((8, 0, 0), (24, 0, 112)):
+        cfg = gen.cfg2(T, off=off, cnt=cnt)
+        hid = torch.from_numpy(cfg["hidden"].view(np.int16)).cuda()
+        bias = torch.from_numpy(cfg["bias"]).cuda()
+        ref = mr.router_gemm_route(hid, w_dev, bias, local_offset=off, local_count=cnt, want_ids=True)
+        torch.cuda.synchronize()
+        ref = {k: v.clone() for k, v in ref.items() if v is not None}
+        out = mr.alloc_outputs(T, 896, 16, cnt, hid.device, True)
+        out["logits"] = torch.empty((T, 896), dtype=torch.float32, device=hid.device)
+        cases.append((hid, bias, off, cnt, ref, out))
+
+    def run(stream=None):
+        for i in range(6):
+            hid, bias, off, cnt, _, out = cases[i % 2]
+            for v in out.values():
+                if v is not None:
+                    v.fill_(-1)
+            mr.router_gemm_route(hid, w_dev, bias, local_offset=off, local_count=cnt, out=out,
+                                 want_ids=True, stream=stream)
+
+    def check():
+        torch.cuda.synchronize()
+        assert mr.device_status() == 0
+        for *_, ref, out in cases:
+            for key, v in ref.items():
+                assert torch.equal(out[key], v), key
+
+    run()
+    check()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        st.wait_stream(torch.cuda.current_stream())
+        run(st)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            run(st)
+    for _ in range(3):
+        for *_, out in cases:
+            for v in out.values():
+                if v is not None:
+                    v.fill_(-7)
+        torch.cuda.synchronize()
+        g.replay()
+        check()
