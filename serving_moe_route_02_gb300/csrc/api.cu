@@ -341,9 +341,19 @@ int moe_route_index(const int32_t* packed, int T, int k, int NE, int32_t* counts
   if (T <= 64) {
     ce = launch_route_decode(a, DT_PACKED, st);
   } else {
-    int grid = (T + 15) / 16;
-    if (grid > d->pw.grid_max) grid = d->pw.grid_max;
-    ce = launch_route_prefill(a, DT_PACKED, d->pw, grid, st);
+    // k = 16 (the Kimi-K3 instance): the approximate-score kernel's ranking, placement
+    // and barriers, reading the packed ids instead of routing (path 3 forces the other)
+    int grid_fast = d->nsm * d->fast_blocks_per_sm;
+    if (grid_fast > d->pw.grid_max) grid_fast = d->pw.grid_max;
+    if (grid_fast > (T + 15) / 16) grid_fast = (T + 15) / 16;
+    if (k == 16 && NE <= kFastBins && NE % 4 == 0 && g_path != 3 && grid_fast >= 1 &&
+        prefill_fast_fits(T, grid_fast)) {
+      ce = launch_route_prefill_fast(a, d->pw, grid_fast, st);
+    } else {
+      int grid = (T + 15) / 16;
+      if (grid > d->pw.grid_max) grid = d->pw.grid_max;
+      ce = launch_route_prefill(a, DT_PACKED, d->pw, grid, st);
+    }
   }
   return ce == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }

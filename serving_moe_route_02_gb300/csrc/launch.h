@@ -54,6 +54,10 @@ bool prefill_fits(int T, int grid);
 // approximate scores (route_prefill_fast.cu).  prefill_fast_fits: T rows on `grid` CTAs
 // fit its per-warp entry room.
 cudaError_t setup_prefill_fast(int* blocks_per_sm);
+// Bins it serves: 896 global ids, or at most 896 rank-local ids plus 16 for the other
+// ranks' slots, rounded up to a multiple of 4.  Index mode (topk_group = 0 in the
+// arguments) takes k = 16 and at most this many bins.
+constexpr int kFastBins = kE + 16;
 bool prefill_fast_fits(int T, int grid);
 cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, int grid,
                                       cudaStream_t st);

@@ -35,10 +35,6 @@ namespace {
 
 __host__ __device__ constexpr int f_align(int x, int a) { return (x + a - 1) / a * a; }
 
-// Bins of the instance this kernel serves: 896 global ids, or at most 896 rank-local ids
-// plus 16 for the other ranks' slots, rounded up to a multiple of 4.
-constexpr int kFastBins = kE + 16;
-
 struct FastSmem {
   static constexpr int NW = 20;                    // warps per CTA
   static constexpr int D = 2;                      // pairs of rows in flight per warp
@@ -79,6 +75,10 @@ static_assert(FastSmem::ROWB % 128 == 0, "row slots keep 128-byte alignment");
 int fast_prefill_rows_per_warp() { return FastSmem::ROWS_PER_WARP; }
 int fast_prefill_warps() { return FastSmem::NW; }
 
+// INDEX: index mode (moe_route_index for k = 16): phase 1 reads the given packed ids of
+// each row (a.logits) instead of routing; an id >= NE, and every occurrence of an id that
+// appears twice in its row, is reported (kErrBadId) and left out of every output.
+template <bool INDEX>
 __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     k_route_prefill_fast(RouteArgs a, PrefillWS pw) {
   using L = FastSmem;
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   }
   for (int i = tid; i < NW * L::WORDS; i += NT) wcnt_all[i] = 0u;
   __syncthreads();
-  if (tid == 0) {
+  if (tid == 0 && !INDEX) {
     mbar_expect_tx(tab_bar, uint32_t(kE * 4));
     bulk_g2s(bias_s, a.bias, kE * 4, tab_bar);
   }
@@ -135,79 +135,129 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     mbar_expect_tx(mb + slot, bytes);
     bulk_g2s(ring + slot * L::SLOTB, logits + size_t(wr0 + 2 * p) * L::ROWB, bytes, mb + slot);
   };
-  if (lane == 0) {
+  if (lane == 0 && !INDEX) {
     for (int d = 0; d < L::D && d < npairs; ++d) issue_pair(d);
   }
   // first row whose wait ran out (-1: none); 0 also when the table never arrived
-  int fail_at = mbar_wait_bounded(tab_bar, 0, a.err) ? -1 : 0;
+  int fail_at = -1;
+  if constexpr (!INDEX) fail_at = mbar_wait_bounded(tab_bar, 0, a.err) ? -1 : 0;
 
-  // error bounds of the approximate scores: the biases' range
-  PairBounds pbnd;
-  {
-    float mx = -INFINITY, mn = INFINITY;
-    for (int e = tid; e < kE; e += NT) {
-      mx = fmaxf(mx, bias_s[e]);
-      mn = fminf(mn, bias_s[e]);
+  const int half = lane >> 4, h = lane & 15;
+  if constexpr (INDEX) {
+    // ---- phase 1 (index mode): the warp's rows two at a time (lanes 0-15 and 16-31),
+    //      all of its (at most 12) pairs' loads in flight at once; ranks as in routing
+    constexpr int kPairs = (L::ROWS_PER_WARP + 1) / 2;
+    __syncthreads();
+    for (int p0 = 0; p0 < npairs; p0 += kPairs) {
+      uint32_t v[kPairs];
+#pragma unroll
+      for (int u = 0; u < kPairs; ++u) {
+        const int i = 2 * (p0 + u) + half;
+        v[u] = (p0 + u < npairs && i < nw)
+                   ? uint32_t(__ldg(static_cast<const int32_t*>(a.logits) + size_t(wr0 + i) * K + h))
+                   : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < kPairs; ++u) {
+        if (p0 + u >= npairs) break;  // uniform over the warp
+        const int i = 2 * (p0 + u) + half;
+        const bool valid = i < nw;
+        const int lid = int(v[u] >> 16);
+        // ids must be distinct within a row (the ranks count rows per id): the same id in
+        // two lanes of one half is a repeat
+        const uint32_t same = __match_any_sync(0xffffffffu, uint32_t(lid) | (uint32_t(half) << 16));
+        const bool ok = valid && lid < a.NE && __popc(same) == 1;
+        if (valid && !ok) atomicExch(a.err, kErrBadId);
+        // ranks: the first row's entries before the second row's
+        const uint32_t sh = uint32_t(lid & 1) * 16u;
+        if (half == 0) {
+          uint16_t e = 0xFFFFu;
+          if (ok) {
+            const uint32_t old = atomicAdd(wcnt + (lid >> 1), 1u << sh);
+            e = static_cast<uint16_t>(uint32_t(lid) | (((old >> sh) & 0xFFFFu) << 10));
+          }
+          ent[i * K + h] = e;
+        }
+        __syncwarp();
+        if (half == 1 && valid) {
+          uint16_t e = 0xFFFFu;
+          if (ok) {
+            const uint32_t old = atomicAdd(wcnt + (lid >> 1), 1u << sh);
+            e = static_cast<uint16_t>(uint32_t(lid) | (((old >> sh) & 0xFFFFu) << 10));
+          }
+          ent[i * K + h] = e;
+        }
+        __syncwarp();
+      }
     }
-    // order-preserving keys, so that integer reductions give the float max and min
-    const uint32_t kmx = __reduce_max_sync(0xffffffffu, fkey(mx));
-    const uint32_t kmn = __reduce_min_sync(0xffffffffu, fkey(mn));
-    if (lane == 0) {
-      tmp[w] = int(kmx);
-      tmp[NW + w] = int(kmn);
+  } else {
+    // error bounds of the approximate scores: the biases' range
+    PairBounds pbnd;
+    {
+      float mx = -INFINITY, mn = INFINITY;
+      for (int e = tid; e < kE; e += NT) {
+        mx = fmaxf(mx, bias_s[e]);
+        mn = fminf(mn, bias_s[e]);
+      }
+      // order-preserving keys, so that integer reductions give the float max and min
+      const uint32_t kmx = __reduce_max_sync(0xffffffffu, fkey(mx));
+      const uint32_t kmn = __reduce_min_sync(0xffffffffu, fkey(mn));
+      if (lane == 0) {
+        tmp[w] = int(kmx);
+        tmp[NW + w] = int(kmn);
+      }
+      __syncthreads();
+      uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
+  #pragma unroll
+      for (int i = 0; i < NW; ++i) {
+        bmx = max(bmx, uint32_t(tmp[i]));
+        bmn = min(bmn, uint32_t(tmp[NW + i]));
+      }
+      pbnd = pair_bounds(a.eps_half, fkey_inv(bmn), fkey_inv(bmx));
+    }
+    // c'' in the pair order route_pair reads: lane h's word j pairs expert 56 h + j with
+    // expert 56 h + 28 + j
+    for (int e = tid; e < kE; e += NT) {
+      const int hh = e / kPairEPL, r = e - hh * kPairEPL;
+      const int c = r >= kChain ? 1 : 0, j = r - c * kChain;
+      cpp_s[hh * kCppStride + 2 * j + c] = __fadd_rn(bias_s[e], pbnd.d0);
     }
     __syncthreads();
-    uint32_t bmx = 0u, bmn = 0xFFFFFFFFu;
-#pragma unroll
-    for (int i = 0; i < NW; ++i) {
-      bmx = max(bmx, uint32_t(tmp[i]));
-      bmn = min(bmn, uint32_t(tmp[NW + i]));
-    }
-    pbnd = pair_bounds(a.eps_half, fkey_inv(bmn), fkey_inv(bmx));
-  }
-  // c'' in the pair order route_pair reads: lane h's word j pairs expert 56 h + j with
-  // expert 56 h + 28 + j
-  for (int e = tid; e < kE; e += NT) {
-    const int hh = e / kPairEPL, r = e - hh * kPairEPL;
-    const int c = r >= kChain ? 1 : 0, j = r - c * kChain;
-    cpp_s[hh * kCppStride + 2 * j + c] = __fadd_rn(bias_s[e], pbnd.d0);
-  }
-  __syncthreads();
 
-  // ---- phase 1: route this warp's rows two at a time, rank their entries within the warp
-  const int half = lane >> 4, h = lane & 15;
-  for (int p = 0; p < npairs && fail_at < 0; ++p) {
-    const int slot = p % L::D;
-    const uint32_t par = uint32_t(p / L::D) & 1u;
-    if (!mbar_wait_bounded(mb + slot, par, a.err)) {
-      fail_at = p;
-      break;
-    }
-    const uint8_t* r0p = ring + slot * L::SLOTB;
-    const bool has1 = 2 * p + 1 < nw;
-    const SlotOut o = route_pair(r0p, has1 ? r0p + L::ROWB : r0p, bias_s, cpp_s, a.stab, pbnd, a, wsp[w]);
-    const int i = 2 * p + half;  // this half's row within the warp
-    const bool valid = i < nw;
-    const int t = wr0 + i;
-    if (valid) {
-      a.packed[size_t(t) * K + h] = o.packed;
-      if (a.ids) a.ids[size_t(t) * K + h] = o.id;
-    }
-    // ranks: the first row's entries before the second row's
-    const uint32_t sh = uint32_t(o.lid & 1) * 16u;
-    if (half == 0) {
-      const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
-      ent[i * K + h] = static_cast<uint16_t>(uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 10));
-    }
-    __syncwarp();
-    if (half == 1 && valid) {
-      const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
-      ent[i * K + h] = static_cast<uint16_t>(uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 10));
-    }
-    __syncwarp();
-    if (lane == 0 && p + L::D < npairs) {
-      fence_proxy_async_smem();
-      issue_pair(p + L::D);
+    // ---- phase 1: route this warp's rows two at a time, rank their entries within the warp
+    for (int p = 0; p < npairs && fail_at < 0; ++p) {
+      const int slot = p % L::D;
+      const uint32_t par = uint32_t(p / L::D) & 1u;
+      if (!mbar_wait_bounded(mb + slot, par, a.err)) {
+        fail_at = p;
+        break;
+      }
+      const uint8_t* r0p = ring + slot * L::SLOTB;
+      const bool has1 = 2 * p + 1 < nw;
+      const SlotOut o = route_pair(r0p, has1 ? r0p + L::ROWB : r0p, bias_s, cpp_s, a.stab, pbnd, a, wsp[w]);
+      const int i = 2 * p + half;  // this half's row within the warp
+      const bool valid = i < nw;
+      const int t = wr0 + i;
+      if (valid) {
+        a.packed[size_t(t) * K + h] = o.packed;
+        if (a.ids) a.ids[size_t(t) * K + h] = o.id;
+      }
+      // ranks: the first row's entries before the second row's
+      const uint32_t sh = uint32_t(o.lid & 1) * 16u;
+      if (half == 0) {
+        const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
+        ent[i * K + h] = static_cast<uint16_t>(uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 10));
+      }
+      __syncwarp();
+      if (half == 1 && valid) {
+        const uint32_t old = atomicAdd(wcnt + (o.lid >> 1), 1u << sh);
+        ent[i * K + h] = static_cast<uint16_t>(uint32_t(o.lid) | (((old >> sh) & 0xFFFFu) << 10));
+      }
+      __syncwarp();
+      if (lane == 0 && p + L::D < npairs) {
+        fence_proxy_async_smem();
+        issue_pair(p + L::D);
+      }
     }
   }
   // after a wait that ran out, the copies issued for pairs fail_at .. fail_at + D - 1 may
@@ -245,6 +295,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     for (int x = lane; x < nrouted * K; x += 32) {
       const uint32_t v = ent[x];
       const int l = int(v & 0x3FFu);
+      if (INDEX && l >= a.NE) continue;  // an id left out (index mode)
       const uint32_t wp = (wcnt[l >> 1] >> (uint32_t(l & 1) * 16u)) & 0xFFFFu;
       const int lp = lbase_s[l] + int(wp) + int(v >> 10);
       sval[lp] = (wr0 + x / K) * K + (x % K);
@@ -296,6 +347,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     for (int x = lane; x < nrouted * K; x += 32) {
       const uint32_t v = ent[x];
       const int l = int(v & 0x3FFu);
+      if (INDEX && l >= a.NE) continue;
       const uint32_t wp = (wcnt[l >> 1] >> (uint32_t(l & 1) * 16u)) & 0xFFFFu;
       a.inv[size_t(wr0) * K + x] = gbase_s[l] + lbase_s[l] + int(wp) + int(v >> 10);
     }
@@ -304,10 +356,13 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
 }
 
 cudaError_t setup_prefill_fast(int* blocks_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(k_route_prefill_fast, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k_route_prefill_fast<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        FastSmem::total);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_route_prefill_fast,
+  e = cudaFuncSetAttribute(k_route_prefill_fast<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           FastSmem::total);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_route_prefill_fast<false>,
                                                        FastSmem::NW * 32, FastSmem::total);
 }
 
@@ -320,8 +375,9 @@ bool prefill_fast_fits(int T, int grid) {
 
 cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, int grid,
                                       cudaStream_t st) {
-  if (!prefill_fast_fits(a.T, grid) || a.k != 16 || a.Kg != 4 || a.NE > kFastBins)
-    return cudaErrorInvalidValue;
+  if (!prefill_fast_fits(a.T, grid) || a.k != 16 || a.NE > kFastBins) return cudaErrorInvalidValue;
+  const bool index = a.Kg == 0;  // moe_route_index sets topk_group 0
+  if (!index && a.Kg != 4) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(FastSmem::NW * 32, 1, 1);
@@ -332,7 +388,8 @@ cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, i
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_route_prefill_fast, a, ws);
+  return index ? cudaLaunchKernelEx(&cfg, k_route_prefill_fast<true>, a, ws)
+               : cudaLaunchKernelEx(&cfg, k_route_prefill_fast<false>, a, ws);
 }
 
 // ------------------------------------------------------------ approximation error

@@ -80,12 +80,13 @@ def test_index_reports_bad_id(mr, T, fault):
 
 
 @pytest.mark.parametrize("T", [16, 5000])
-def test_index_leaves_out_every_bad_entry(mr, T):
-    """Rows with an id repeated three times, a repeated pair and an id >= NE: both kernels
-    leave out exactly those entries (every occurrence of a repeated id), so the counts
-    are the histogram of the remaining ones and the permutation holds exactly them."""
-    k, NE = 8, 40
-    ids = distinct_rows(T, k, NE, 4200 + T)
+@pytest.mark.parametrize("k,NE", [(8, 40), (16, 896), (16, 128)])
+def test_index_leaves_out_every_bad_entry(mr, T, k, NE):
+    """Rows with an id repeated three times, a repeated pair and an id >= NE: every kernel
+    (decode-size, and for T > 64 the exact-score one or, at k = 16, the approximate-score
+    one) leaves out exactly those entries (every occurrence of a repeated id), so the
+    counts are the histogram of the remaining ones and the permutation holds exactly them."""
+    ids = distinct_rows(T, k, NE, 4200 + T + k)
     bad_rows = sorted({1, T // 3, T // 2, T - 1})
     ids[bad_rows[0], 2] = ids[bad_rows[0], 5] = ids[bad_rows[0], 0]   # three times
     ids[bad_rows[1], 7] = ids[bad_rows[1], 3]                         # a pair
