@@ -346,8 +346,8 @@ int moe_route_index(const int32_t* packed, int T, int k, int NE, int32_t* counts
     int grid_fast = d->nsm * d->fast_blocks_per_sm;
     if (grid_fast > d->pw.grid_max) grid_fast = d->pw.grid_max;
     if (grid_fast > (T + 15) / 16) grid_fast = (T + 15) / 16;
-    if (k == 16 && NE <= kFastBins && NE % 4 == 0 && g_path != 3 && grid_fast >= 1 &&
-        prefill_fast_fits(T, grid_fast)) {
+    if (k == 16 && NE <= kFastBins && NE % 4 == 0 && reinterpret_cast<uintptr_t>(packed) % 16 == 0 &&
+        g_path != 3 && grid_fast >= 1 && prefill_fast_fits(T, grid_fast)) {
       ce = launch_route_prefill_fast(a, d->pw, grid_fast, st);
     } else {
       int grid = (T + 15) / 16;

@@ -76,8 +76,9 @@ int fast_prefill_rows_per_warp() { return FastSmem::ROWS_PER_WARP; }
 int fast_prefill_warps() { return FastSmem::NW; }
 
 // INDEX: index mode (moe_route_index for k = 16): phase 1 reads the given packed ids of
-// each row (a.logits) instead of routing; an id >= NE, and every occurrence of an id that
-// appears twice in its row, is reported (kErrBadId) and left out of every output.
+// each row (a.logits, 16-byte aligned: each warp's rows come in one bulk copy) instead of
+// routing; an id >= NE, and every occurrence of an id that appears twice in its row, is
+// reported (kErrBadId) and left out of every output.
 template <bool INDEX>
 __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     k_route_prefill_fast(RouteArgs a, PrefillWS pw) {
@@ -138,56 +139,56 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   if (lane == 0 && !INDEX) {
     for (int d = 0; d < L::D && d < npairs; ++d) issue_pair(d);
   }
+  if (INDEX && lane == 0 && nw > 0) {
+    // index mode: the warp's rows of packed ids (64 bytes each) in one bulk copy
+    const uint32_t bytes = uint32_t(nw) * K * 4;
+    mbar_expect_tx(mb, bytes);
+    bulk_g2s(ring, static_cast<const uint8_t*>(a.logits) + size_t(wr0) * K * 4, bytes, mb);
+  }
   // first row whose wait ran out (-1: none); 0 also when the table never arrived
   int fail_at = -1;
   if constexpr (!INDEX) fail_at = mbar_wait_bounded(tab_bar, 0, a.err) ? -1 : 0;
 
   const int half = lane >> 4, h = lane & 15;
   if constexpr (INDEX) {
-    // ---- phase 1 (index mode): the warp's rows two at a time (lanes 0-15 and 16-31),
-    //      all of its (at most 12) pairs' loads in flight at once; ranks as in routing
-    constexpr int kPairs = (L::ROWS_PER_WARP + 1) / 2;
+    // ---- phase 1 (index mode): the warp's rows two at a time (lanes 0-15 and 16-31)
+    //      from its bulk copy; ranks as in routing
     __syncthreads();
-    for (int p0 = 0; p0 < npairs; p0 += kPairs) {
-      uint32_t v[kPairs];
-#pragma unroll
-      for (int u = 0; u < kPairs; ++u) {
-        const int i = 2 * (p0 + u) + half;
-        v[u] = (p0 + u < npairs && i < nw)
-                   ? uint32_t(__ldg(static_cast<const int32_t*>(a.logits) + size_t(wr0 + i) * K + h))
-                   : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < kPairs; ++u) {
-        if (p0 + u >= npairs) break;  // uniform over the warp
-        const int i = 2 * (p0 + u) + half;
+    if (nw > 0 && !mbar_wait_bounded(mb, 0, a.err)) fail_at = 0;
+    const uint32_t* ids = reinterpret_cast<const uint32_t*>(ring);
+    {
+      for (int p = 0; p < npairs && fail_at < 0; ++p) {
+        const int i = 2 * p + half;
         const bool valid = i < nw;
-        const int lid = int(v[u] >> 16);
-        // ids must be distinct within a row (the ranks count rows per id): the same id in
-        // two lanes of one half is a repeat
-        const uint32_t same = __match_any_sync(0xffffffffu, uint32_t(lid) | (uint32_t(half) << 16));
-        const bool ok = valid && lid < a.NE && __popc(same) == 1;
-        if (valid && !ok) atomicExch(a.err, kErrBadId);
-        // ranks: the first row's entries before the second row's
+        const int lid = int((valid ? ids[i * K + h] : 0u) >> 16);
+        const bool inr = valid && lid < a.NE;
         const uint32_t sh = uint32_t(lid & 1) * 16u;
-        if (half == 0) {
-          uint16_t e = 0xFFFFu;
-          if (ok) {
-            const uint32_t old = atomicAdd(wcnt + (lid >> 1), 1u << sh);
-            e = static_cast<uint16_t>(uint32_t(lid) | (((old >> sh) & 0xFFFFu) << 10));
+        // ranks: the first row's entries before the second row's.  Ids must be distinct
+        // within a row (the ranks count rows per id): after a row's increments, a lane whose
+        // counter rose by more than one shares its id with another lane of the row (in
+        // every repeat the lane that counted first sees it); only then is every occurrence
+        // found (a match over the half) and its increments taken back.
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const bool mine = half == hh && inr;
+          uint32_t old = 0u;
+          if (mine) old = atomicAdd(wcnt + (lid >> 1), 1u << sh);
+          __syncwarp();
+          const uint32_t rank = (old >> sh) & 0xFFFFu;
+          const bool suspect = mine && ((wcnt[lid >> 1] >> sh) & 0xFFFFu) - rank != 1u;
+          bool dup = false;
+          if (__any_sync(0xffffffffu, suspect)) {
+            const uint32_t same = __match_any_sync(0xffffffffu, uint32_t(lid) | (uint32_t(half) << 16));
+            dup = mine && __popc(same) > 1;
+            __syncwarp();
+            if (dup) atomicSub(wcnt + (lid >> 1), 1u << sh);
           }
-          ent[i * K + h] = e;
-        }
-        __syncwarp();
-        if (half == 1 && valid) {
-          uint16_t e = 0xFFFFu;
-          if (ok) {
-            const uint32_t old = atomicAdd(wcnt + (lid >> 1), 1u << sh);
-            e = static_cast<uint16_t>(uint32_t(lid) | (((old >> sh) & 0xFFFFu) << 10));
+          if (half == hh && valid) {
+            if (!inr || dup) atomicExch(a.err, kErrBadId);
+            ent[i * K + h] = (inr && !dup) ? static_cast<uint16_t>(uint32_t(lid) | (rank << 10)) : uint16_t(0xFFFFu);
           }
-          ent[i * K + h] = e;
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
   } else {
@@ -263,9 +264,13 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   // after a wait that ran out, the copies issued for pairs fail_at .. fail_at + D - 1 may
   // still be owed to the ring: wait for them (bounded) before the ring is reused
   if (fail_at >= 0 && lane == 0) {
-    if (w == 0) mbar_wait_bounded(tab_bar, 0, nullptr);
-    for (int q = fail_at; q < npairs && q < fail_at + L::D; ++q)
-      mbar_wait_bounded(mb + q % L::D, uint32_t(q / L::D) & 1u, nullptr);
+    if (INDEX) {
+      if (nw > 0) mbar_wait_bounded(mb, 0, nullptr);  // the one bulk copy of index mode
+    } else {
+      if (w == 0) mbar_wait_bounded(tab_bar, 0, nullptr);
+      for (int q = fail_at; q < npairs && q < fail_at + L::D; ++q)
+        mbar_wait_bounded(mb + q % L::D, uint32_t(q / L::D) & 1u, nullptr);
+    }
   }
   __syncthreads();
 

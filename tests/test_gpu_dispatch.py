@@ -43,6 +43,25 @@ def test_index_of_routed_packed(mr, T, off, cnt):
         assert np.array_equal(idx[key].cpu().numpy(), ref[key]), key
 
 
+def test_index_of_unaligned_packed(mr):
+    """Packed values 4 bytes off a 16-byte boundary (the approximate-score kernel copies
+    aligned rows, so the exact-score kernel takes them): the same outputs as the oracle."""
+    T = 5000
+    cfg = gen.cfg3(T)
+    out = routed(mr, cfg)
+    NE = out["counts"].numel()
+    buf = torch.empty(T * 16 + 1, dtype=torch.int32, device="cuda")
+    view = buf[1:].view(T, 16)
+    view.copy_(out["packed"])
+    assert view.data_ptr() % 16 == 4
+    idx = mr.route_index(view, NE)
+    torch.cuda.synchronize()
+    assert mr.device_status() == 0
+    ref = oracle.route_index(out["packed"].cpu().numpy(), NE)
+    for key in ("counts", "offsets", "perm"):
+        assert np.array_equal(idx[key].cpu().numpy(), ref[key]), key
+
+
 def distinct_rows(T, k, NE, seed):
     """T rows of k distinct ids below NE: the k smallest of NE seeded draws per row."""
     r = gen.raw64(seed, T * NE).reshape(T, NE)
