@@ -384,6 +384,38 @@ def layout_timing(torch, mr, dev, out, T, tile=128, reps=50, replays=10, bufs=No
             "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
 
 
+def index_timing(torch, mr, dev, out, reps=20, replays=10):
+    """moe_route_index on the routing's own packed ids (T rows, k = 16): µs per call under
+    CUDA-graph replay, and whether its counts, offsets and perm equal the routing's."""
+    NE = out["counts"].numel()
+    idx = mr.route_index(out["packed"], NE)
+    st = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(st):
+        st.wait_stream(torch.cuda.current_stream(dev))
+        mr.route_index(out["packed"], NE, out=idx, stream=st)
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for _ in range(reps):
+                mr.route_index(out["packed"], NE, out=idx, stream=st)
+        g.replay()
+        st.synchronize()
+        samples = []
+        for _ in range(replays):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            g.replay()
+            b.record(st)
+            b.synchronize()
+            samples.append(a.elapsed_time(b) * 1e3 / reps)
+    same = all(torch.equal(idx[k], out[k]) for k in ("counts", "offsets", "perm"))
+    T = out["packed"].shape[0]
+    return {"T": T, "us_per_call": round(statistics.median(samples), 3), "timing": "CUDA-graph replay",
+            "equals_routing": same,
+            "algorithmic_bytes": T * 16 * 4 + T * 16 * 4 + 4 * (2 * NE + 1)}
+
+
 def run_case(torch, mr, dev, args, T=64):
     """Plain launches of one path, for ncu captures: decode routing or contraction +
     routing at 64 rows, or the expert-GEMM layout / the index of packed ids at 65,536
@@ -560,11 +592,12 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt[0])
 
-    decode = gemm = layout = None
+    decode = gemm = layout = index = None
     if rank == 0 and not (args.no_decode or args.quick):
         decode = decode_latency(torch, mr, dev)
         gemm = gemm_route_latency(torch, mr, dev)
         layout = layout_timing(torch, mr, dev, outs[0], T_PREFILL, bufs=bufs, bias=bias)
+        index = index_timing(torch, mr, dev, outs[0])
 
     peaks, peak_src = measured_peaks()
     ab = algorithmic_bytes(T_PREFILL)
@@ -604,6 +637,8 @@ def main():
         line["router_gemm_route"] = gemm
     if layout is not None:
         line["route_layout"] = layout
+    if index is not None:
+        line["route_index"] = index
     if rank == 0 and not (args.no_cpu_baseline or args.quick):
         line["cpu_baseline"] = cpu_baseline()
     if world > 1:
