@@ -326,9 +326,22 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   }
 
   // ---- phase 3: offsets, then the sorted entries to perm, one run per bin
-  for (int e = tid; e < a.NE; e += NT) {
-    hist_s[e] = __ldcg(pw.counts + e);
-    gbase_s[e] = __ldcg(pw.prefix + size_t(e) * pw.grid_max + cta);
+  {
+    // at most two bins per thread (NE <= 912 < 2 NT): all four loads in flight at once
+    static_assert(kFastBins <= 2 * NT, "two bins per thread cover the bins");
+    const int e0 = tid, e1 = tid + NT;
+    const int c0 = e0 < a.NE ? __ldcg(pw.counts + e0) : 0;
+    const int c1 = e1 < a.NE ? __ldcg(pw.counts + e1) : 0;
+    const int g0 = e0 < a.NE ? __ldcg(pw.prefix + size_t(e0) * pw.grid_max + cta) : 0;
+    const int g1 = e1 < a.NE ? __ldcg(pw.prefix + size_t(e1) * pw.grid_max + cta) : 0;
+    if (e0 < a.NE) {
+      hist_s[e0] = c0;
+      gbase_s[e0] = g0;
+    }
+    if (e1 < a.NE) {
+      hist_s[e1] = c1;
+      gbase_s[e1] = g1;
+    }
   }
   __syncthreads();
   int* off_s = reinterpret_cast<int*>(smem + L::o_ws);  // the routing scratch is free
