@@ -22,6 +22,8 @@
 //   CTAs that own bins of the scan place their entries after it, before they wait).
 // Phase 3: offsets from the totals (CTA 0 writes counts and offsets); the sorted buffer
 //   goes to perm in runs of consecutive addresses, one run per bin.
+// Index mode (moe_route_index, k = 16): phase 1 takes each warp's rows of given packed
+//   ids in one bulk copy and only ranks them; everything after it is the same.
 // Every wait is bounded in time; a wait that runs out sets the status word and the CTA
 // leaves (through grid_exit, which restores the barrier words once all CTAs have left).
 #include <cooperative_groups.h>
