@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   const uint8_t* logits = static_cast<const uint8_t*>(a.logits);
   const int nwords = a.NE / 2;  // NE is a multiple of 4
 
+  // the next launch on the stream (a programmatic dependent) may start now: before its
+  // griddepcontrol.wait it touches only its own shared memory
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- setup: mbarriers, counters, score table and bias, first rows in flight
   uint64_t* tab_bar = mbar_all + NW * L::D;
   if (lane == 0) {
@@ -127,6 +130,9 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   }
   for (int i = tid; i < NW * L::WORDS; i += NT) wcnt_all[i] = 0u;
   __syncthreads();
+  // inputs, outputs, the workspace and the grid barrier's words belong to the preceding
+  // launch until it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (tid == 0 && !INDEX) {
     mbar_expect_tx(tab_bar, uint32_t(kE * 4));
     bulk_g2s(bias_s, a.bias, kE * 4, tab_bar);
@@ -403,11 +409,13 @@ cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, i
   cfg.blockDim = dim3(FastSmem::NW * 32, 1, 1);
   cfg.dynamicSmemBytes = FastSmem::total;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return index ? cudaLaunchKernelEx(&cfg, k_route_prefill_fast<true>, a, ws)
                : cudaLaunchKernelEx(&cfg, k_route_prefill_fast<false>, a, ws);
 }
