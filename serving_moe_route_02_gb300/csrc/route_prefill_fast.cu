@@ -71,6 +71,59 @@ static_assert(FastSmem::ROWS_PER_WARP <= 64, "a rank within a warp fits 6 bits")
 static_assert(kFastBins <= 1024, "an id fits 10 bits");
 static_assert(2 * FastSmem::NW + 2 <= 64, "the bias range reduction and the barrier flag fit tmp");
 static_assert(FastSmem::ROWB % 128 == 0, "row slots keep 128-byte alignment");
+static_assert(160 * FastSmem::NW * 4 <= FastSmem::NW * FastSmem::D * FastSmem::SLOTB,
+              "the column scan's tile for up to 160 CTAs fits the ring");
+
+// Column scan over CTAs for the bins this CTA owns (warp w: bin blockIdx.x * NW + w, and
+// further chunks grid * NW bins apart; called by every thread of every CTA): totals go to
+// counts[e], and each CTA's exclusive prefix to the CTA-major matrix
+// prefix[c * kMaxBins + e] through a [grid][NW] tile in shared memory (`tile`), so that a
+// chunk's prefixes leave as one contiguous piece per CTA and phase 3 reads its own row of
+// the matrix contiguously.
+__device__ __forceinline__ void column_scan_cta_major(const PrefillWS& pw, int NE, int grid, int* tile) {
+  constexpr int NW = FastSmem::NW, NT = NW * 32;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e0 = int(blockIdx.x) * NW; e0 < NE; e0 += grid * NW) {  // uniform over the CTA
+    const int e = e0 + w;
+    if (e < NE) {
+      const int* hrow = pw.hist + size_t(e) * pw.grid_max;
+      int carry = 0;
+      for (int c0 = 0; c0 < grid; c0 += 256) {
+        const int span = min(256, grid - c0);
+        const int per = (span + 31) / 32;
+        const int cl = c0 + lane * per;
+        int v[8];
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[i] = (i < per && cl + i < c0 + span) ? __ldcg(hrow + cl + i) : 0;
+          sum += v[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        int run = carry + incl - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < per && cl + i < c0 + span) tile[(cl + i) * NW + w] = run;
+          run += v[i];
+        }
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) pw.counts[e] = carry;
+    }
+    __syncthreads();
+    const int nb = min(NW, NE - e0);
+    for (int x = threadIdx.x; x < grid * nb; x += NT) {
+      const int c = x / nb, j = x - c * nb;
+      pw.prefix[size_t(c) * kMaxBins + e0 + j] = tile[c * NW + j];
+    }
+    __syncthreads();
+  }
+}
 
 }  // namespace
 
@@ -325,7 +378,8 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     grid_exit(pw.bar, grid);
     return;
   }
-  column_scan(pw, a.NE, grid, NW);
+  // the ring is free in the CTAs that scan: they place their entries afterwards
+  column_scan_cta_major(pw, a.NE, grid, reinterpret_cast<int*>(ring_all));
   const unsigned arrival2 = grid_arrive(pw.bar, grid);
   if (scanner) place();
   if (!grid_wait(pw.bar, arrival2, a.err, flag_s, a.barrier_wait_ns)) {
@@ -340,8 +394,8 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     const int e0 = tid, e1 = tid + NT;
     const int c0 = e0 < a.NE ? __ldcg(pw.counts + e0) : 0;
     const int c1 = e1 < a.NE ? __ldcg(pw.counts + e1) : 0;
-    const int g0 = e0 < a.NE ? __ldcg(pw.prefix + size_t(e0) * pw.grid_max + cta) : 0;
-    const int g1 = e1 < a.NE ? __ldcg(pw.prefix + size_t(e1) * pw.grid_max + cta) : 0;
+    const int g0 = e0 < a.NE ? __ldcg(pw.prefix + size_t(cta) * kMaxBins + e0) : 0;
+    const int g1 = e1 < a.NE ? __ldcg(pw.prefix + size_t(cta) * kMaxBins + e1) : 0;
     if (e0 < a.NE) {
       hist_s[e0] = c0;
       gbase_s[e0] = g0;
