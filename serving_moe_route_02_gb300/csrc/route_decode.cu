@@ -441,6 +441,8 @@ static cudaError_t launch_decode_t(cudaLaunchConfig_t& cfg, const RouteArgs& a) 
 cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) {
   if (a.T > kDecodeMaxRows) return cudaErrorInvalidValue;
   const int ctas = decode_ctas(a.T);
+  // a CTA's row buffer and warps hold at most kDecodeRowsPerCta rows
+  if (ctas < 1 || (a.T + ctas - 1) / ctas > kDecodeRowsPerCta) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
