@@ -354,32 +354,38 @@ def layout_timing(torch, mr, dev, out, T, tile=128, reps=50, replays=10, bufs=No
     us_padded = replay_us(dict(L, inv_perm=None))
     # the inverse map written by the routing instead (moe_route_ex): its extra cost per
     # 65,536-row routing call, plain launches over the rotating input buffers
-    extra = None
+    extra = extra_layout = None
     if bufs is not None:
         inv = torch.empty(T * K, dtype=torch.int32, device=dev)
         outx = mr.alloc_outputs(T, E, K, 0, dev)
 
-        def route_us(with_inv, n=30):
+        def route_us(with_inv, n=30, tile=None):
             o = dict(outx, inv_perm=inv if with_inv else None)
+            if tile is not None:
+                o.update(padded_offsets=L["padded_offsets"], padded_rows=L["padded_rows"],
+                         m_indices=L["m_indices"])
             for i in range(3):
-                mr.route(bufs[i % len(bufs)], bias, out=o)
+                mr.route(bufs[i % len(bufs)], bias, out=o, layout_tile=tile)
             torch.cuda.synchronize()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
             for i in range(n):
-                mr.route(bufs[i % len(bufs)], bias, out=o)
+                mr.route(bufs[i % len(bufs)], bias, out=o, layout_tile=tile)
             b.record()
             b.synchronize()
             return a.elapsed_time(b) * 1e3 / n
 
-        extra = round(route_us(True) - route_us(False), 3)
+        base = route_us(False)
+        extra = round(route_us(True) - base, 3)
+        extra_layout = round(route_us(True, tile=tile) - base, 3)
     nbytes = 4 * n + 4 * n + 2 * 4 * cap + 4 * (2 * NE + 1) + 4 * (NE + 1)
     peaks, _ = measured_peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
     return {"T": T, "tile": tile, "capacity": cap, "us_per_call": round(us, 3),
             "us_per_call_without_inverse": round(us_padded, 3),
-            "routing_extra_us_for_inverse": extra, "timing": "CUDA-graph replay",
+            "routing_extra_us_for_inverse": extra,
+            "routing_extra_us_for_inverse_and_layout": extra_layout, "timing": "CUDA-graph replay",
             "algorithmic_bytes": nbytes, "gbs": round(gbs, 1),
             "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3)}
 

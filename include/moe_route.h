@@ -114,6 +114,26 @@ int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T,
                  int32_t* topk_ids, int32_t* inv_perm, struct CUstream_st* stream);
 
 /*
+ * moe_route_with_layout -- moe_route_ex and then moe_route_layout (without its inverse
+ * map: inv_perm here is moe_route_ex's) in one call: the routing plus the expert-GEMM
+ * layout that moe_route_layout defines, for a tile of `tile` rows.
+ *   tile >= 1; padded_offsets [NE + 1] out, nullable; padded_rows [capacity] and
+ *   m_indices [capacity] out, nullable, with capacity >= moe_route_padded_capacity(T, k,
+ *   NE, tile) when either is given (all `capacity` rows are written).
+ * Where the bf16 prefill kernel for k = 16 and topk_group = 4 routes the batch, that
+ * kernel writes the layout itself in the same launch; otherwise the layout kernel
+ * follows the routing on the stream.  The results are the same either way.
+ * Errors: those of moe_route; INVALID_ARG for tile < 1, a capacity below the bound or a
+ * bound beyond 2^31 - 1.  All layout outputs NULL: the same as moe_route_ex.
+ */
+int moe_route_with_layout(const void* logits, int logits_dtype, const float* bias, int T, int E,
+                          int k, int n_group, int topk_group, float scale, int local_offset,
+                          int local_count, int32_t* packed, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* topk_ids, int32_t* inv_perm, int tile,
+                          int32_t* padded_offsets, int32_t* padded_rows, int32_t* m_indices,
+                          int capacity, struct CUstream_st* stream);
+
+/*
  * moe_route_quant -- the fused route+quant decode launch: moe_route for a decode batch of
  * T <= MOE_ROUTE_QUANT_MAX_TOKENS rows and, in the same kernel launch, the MXFP4
  * quantisation of the batch's activations x that the routed MXFP4 MoE consumes.  The

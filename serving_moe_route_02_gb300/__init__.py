@@ -50,6 +50,9 @@ def load(path: str | None = None):
     lib.moe_route.restype = I
     lib.moe_route_ex.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
     lib.moe_route_ex.restype = I
+    lib.moe_route_with_layout.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, P, P, P, P, P, I, P, P, P,
+                                          I, P]
+    lib.moe_route_with_layout.restype = I
     lib.moe_router_gemm_route.argtypes = [P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, P, P, P]
     lib.moe_router_gemm_route.restype = I
     lib.moe_route_quant.argtypes = [P, I, P, I, I, I, I, I, F, I, I, P, I, P, P, P, P, P, P, P, P]
@@ -168,10 +171,12 @@ def _dtype_code(t: torch.Tensor) -> int:
 def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int = 8,
           topk_group: int = 4, scale: float = 2.5, local_offset: int = 0, local_count: int = 0,
           out: dict | None = None, want_ids: bool = False, want_inv: bool = False,
-          stream=None) -> dict:
+          layout_tile: int | None = None, stream=None) -> dict:
     """moe_route on a [T, E] CUDA tensor of router logits (float32 or bfloat16); with
     want_inv (or an "inv_perm" tensor in out) moe_route_ex, which also writes the inverse
-    permutation out["inv_perm"]."""
+    permutation out["inv_perm"]; with layout_tile, moe_route_with_layout, which also writes
+    the expert-GEMM layout for that tile: out["padded_offsets"], out["padded_rows"] and
+    out["m_indices"] (allocated at the capacity bound when absent)."""
     if not (logits.is_cuda and bias.is_cuda):
         raise ValueError("logits and bias must be CUDA tensors")
     if not logits.is_contiguous() or not bias.is_contiguous() or bias.dtype != torch.float32:
@@ -181,6 +186,20 @@ def route(logits: torch.Tensor, bias: torch.Tensor, *, k: int = 16, n_group: int
         out = alloc_outputs(T, E, k, local_count, logits.device, want_ids)
     if want_inv and out.get("inv_perm") is None:
         out["inv_perm"] = torch.empty(T * k, dtype=torch.int32, device=logits.device)
+    if layout_tile is not None:
+        NE = out["counts"].numel()
+        cap = padded_capacity(T, k, NE, layout_tile)
+        for key, n in (("padded_offsets", NE + 1), ("padded_rows", cap), ("m_indices", cap)):
+            if out.get(key) is None:
+                out[key] = torch.empty(n, dtype=torch.int32, device=logits.device)
+        rc = load().moe_route_with_layout(
+            _ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group, topk_group, float(scale),
+            local_offset, local_count, _ptr(out["packed"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+            _ptr(out["perm"]), _ptr(out.get("ids")), _ptr(out.get("inv_perm")), layout_tile,
+            _ptr(out["padded_offsets"]), _ptr(out["padded_rows"]), _ptr(out["m_indices"]),
+            out["padded_rows"].numel(), _stream(stream))
+        _check(rc, "moe_route_with_layout")
+        return out
     if out.get("inv_perm") is not None:
         rc = load().moe_route_ex(_ptr(logits), _dtype_code(logits), _ptr(bias), T, E, k, n_group,
                                  topk_group, float(scale), local_offset, local_count,

@@ -156,10 +156,20 @@ int moe_route(const void* logits, int logits_dtype, const float* bias, int T, in
                       local_count, packed, counts, offsets, perm, topk_ids, nullptr, stream);
 }
 
-int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
-                 int n_group, int topk_group, float scale, int local_offset, int local_count,
-                 int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
-                 int32_t* topk_ids, int32_t* inv_perm, struct CUstream_st* stream) {
+namespace {
+
+// The expert-GEMM layout asked of a routing call (moe_route_with_layout), validated.
+struct LayoutReq {
+  int tile, capacity;
+  int32_t* padded_offsets;
+  int32_t* padded_rows;
+  int32_t* m_indices;
+};
+
+int route_impl(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+               int n_group, int topk_group, float scale, int local_offset, int local_count,
+               int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* topk_ids,
+               int32_t* inv_perm, const LayoutReq* lay, struct CUstream_st* stream) {
   int rc = check_route_args(T, E, k, n_group, topk_group, local_offset, local_count);
   if (rc != MOE_ROUTE_OK) return rc;
   if (logits_dtype != MOE_ROUTE_F32 && logits_dtype != MOE_ROUTE_BF16) return MOE_ROUTE_E_INVALID_ARG;
@@ -215,6 +225,15 @@ int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T,
       if (grid_fast > (T + 15) / 16) grid_fast = (T + 15) / 16;
       if (dt == DT_BF16 && k == 16 && topk_group == 4 && g_path != 3 && grid_fast >= 1 &&
           prefill_fast_fits(T, grid_fast)) {
+        if (lay) {
+          // this kernel writes the layout itself
+          a.tile = lay->tile;
+          a.capacity = lay->capacity;
+          a.poffs = lay->padded_offsets;
+          a.prows = lay->padded_rows;
+          a.midx = lay->m_indices;
+          lay = nullptr;
+        }
         ce = launch_route_prefill_fast(a, d->pw, grid_fast, st);
       } else {
         const int grid_cap = d->pw.grid_max;
@@ -225,7 +244,51 @@ int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T,
       }
     }
   }
+  if (ce == cudaSuccess && lay) {
+    // elsewhere the layout kernel follows the routing on the stream
+    LayoutArgs g = {};
+    g.counts = counts;
+    g.offsets = offsets;
+    g.perm = perm;
+    g.n = T * k;
+    g.NE = a.NE;
+    g.tile = lay->tile;
+    g.capacity = lay->capacity;
+    g.padded_offsets = lay->padded_offsets;
+    g.padded_rows = lay->padded_rows;
+    g.m_indices = lay->m_indices;
+    ce = launch_route_layout(g, d->nsm, st);
+  }
   return ce == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
+}
+
+}  // namespace
+
+int moe_route_ex(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,
+                 int n_group, int topk_group, float scale, int local_offset, int local_count,
+                 int32_t* packed, int32_t* counts, int32_t* offsets, int32_t* perm,
+                 int32_t* topk_ids, int32_t* inv_perm, struct CUstream_st* stream) {
+  return route_impl(logits, logits_dtype, bias, T, E, k, n_group, topk_group, scale, local_offset,
+                    local_count, packed, counts, offsets, perm, topk_ids, inv_perm, nullptr, stream);
+}
+
+int moe_route_with_layout(const void* logits, int logits_dtype, const float* bias, int T, int E,
+                          int k, int n_group, int topk_group, float scale, int local_offset,
+                          int local_count, int32_t* packed, int32_t* counts, int32_t* offsets,
+                          int32_t* perm, int32_t* topk_ids, int32_t* inv_perm, int tile,
+                          int32_t* padded_offsets, int32_t* padded_rows, int32_t* m_indices,
+                          int capacity, struct CUstream_st* stream) {
+  int rc = check_route_args(T, E, k, n_group, topk_group, local_offset, local_count);
+  if (rc != MOE_ROUTE_OK) return rc;
+  const int NE = bins(E, k, local_count);
+  const int need = moe_route_padded_capacity(T, k, NE, tile);
+  if (need < 0) return MOE_ROUTE_E_INVALID_ARG;
+  const bool padded = padded_rows || m_indices;
+  if (padded && capacity < need) return MOE_ROUTE_E_INVALID_ARG;
+  LayoutReq lay = {tile, padded ? capacity : 0, padded_offsets, padded_rows, m_indices};
+  return route_impl(logits, logits_dtype, bias, T, E, k, n_group, topk_group, scale, local_offset,
+                    local_count, packed, counts, offsets, perm, topk_ids, inv_perm,
+                    (padded_offsets || padded) ? &lay : nullptr, stream);
 }
 
 int moe_route_quant(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,

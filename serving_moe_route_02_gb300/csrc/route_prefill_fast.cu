@@ -70,6 +70,8 @@ static_assert(FastSmem::ROWS_PER_WARP >= 22, "room for 65,536 rows on 152 SMs");
 static_assert(FastSmem::ROWS_PER_WARP <= 64, "a rank within a warp fits 6 bits");
 static_assert(kFastBins <= 1024, "an id fits 10 bits");
 static_assert(2 * FastSmem::NW + 2 <= 64, "the bias range reduction and the barrier flag fit tmp");
+static_assert(2 * (kFastBins + 1) * 4 <= FastSmem::NW * int(sizeof(PairScratch)),
+              "phase 3's offsets and padded offsets fit the routing scratch");
 static_assert(FastSmem::ROWB % 128 == 0, "row slots keep 128-byte alignment");
 static_assert(160 * FastSmem::NW * 4 <= FastSmem::NW * FastSmem::D * FastSmem::SLOTB,
               "the column scan's tile for up to 160 CTAs fits the ring");
@@ -415,12 +417,48 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     }
     if (tid == 0) a.offsets[a.NE] = off_s[a.NE];
   }
+  // the expert-GEMM layout, when asked: tile-padded offsets (an exclusive scan of the
+  // padded bin sizes, in the routing scratch after the offsets)
+  const bool lay = a.poffs || a.prows || a.midx;
+  int* poff_s = off_s + kFastBins + 1;
+  if (lay) {
+    for (int e = tid; e < a.NE; e += NT) poff_s[e] = (hist_s[e] + a.tile - 1) / a.tile * a.tile;
+    __syncthreads();
+    block_scan_fast(poff_s, poff_s, a.NE, tmp);
+    if (cta == 0 && a.poffs)
+      for (int e = tid; e <= a.NE; e += NT) a.poffs[e] = poff_s[e];
+  }
   // global place of CTA-local position 0 of bin e
   for (int e = tid; e < a.NE; e += NT) gbase_s[e] += off_s[e] - lbase_s[e];
   __syncthreads();
   const int nvalid = lbase_s[a.NE];
+  if (!lay) {
 #pragma unroll 4
-  for (int i = tid; i < nvalid; i += NT) a.perm[gbase_s[sbin[i]] + i] = sval[i];
+    for (int i = tid; i < nvalid; i += NT) a.perm[gbase_s[sbin[i]] + i] = sval[i];
+  } else {
+    // entry at perm position p of bin l goes to padded row p - offsets[l] + padded_offsets[l]
+#pragma unroll 4
+    for (int i = tid; i < nvalid; i += NT) {
+      const int l = sbin[i];
+      const int p = gbase_s[l] + i, v = sval[i];
+      a.perm[p] = v;
+      const int r = p - off_s[l] + poff_s[l];
+      if (a.prows) a.prows[r] = v;
+      if (a.midx) a.midx[r] = l;
+    }
+    // the padding rows of bins cta, cta + grid, ... and a share of the rows past the
+    // padded total
+    for (int e = cta; e < a.NE; e += grid) {
+      for (int r = poff_s[e] + hist_s[e] + tid; r < poff_s[e + 1]; r += NT) {
+        if (a.prows) a.prows[r] = -1;
+        if (a.midx) a.midx[r] = -1;
+      }
+    }
+    for (int r = poff_s[a.NE] + cta * NT + tid; r < a.capacity; r += grid * NT) {
+      if (a.prows) a.prows[r] = -1;
+      if (a.midx) a.midx[r] = -1;
+    }
+  }
   if (a.inv) {
     // each entry's place in perm, in token order (coalesced): warp prefix + rank within
     // the warp give its CTA-local position, gbase the rest

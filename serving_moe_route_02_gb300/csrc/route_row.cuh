@@ -33,6 +33,13 @@ struct RouteArgs {
   int32_t* perm;          // [T * k]
   int32_t* ids;           // [T, k] or nullptr
   int32_t* inv = nullptr; // [T * k] or nullptr: position of entry t * k + j in perm
+  // the expert-GEMM layout written by the routing itself (moe_route_with_layout), where
+  // the kernel supports it: tile-padded offsets [NE + 1], padded rows and their bins
+  // [capacity] (-1 for padding); all nullptr when not asked
+  int32_t* poffs = nullptr;
+  int32_t* prows = nullptr;
+  int32_t* midx = nullptr;
+  int tile = 1, capacity = 0;
   int* err;               // device status word
   int T, k, Kg, off, cnt, NE;
   float scale;

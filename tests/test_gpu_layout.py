@@ -168,3 +168,46 @@ def test_routing_writes_the_inverse(mr, cfg, path):
     assert np.array_equal(perm[inv], np.arange(perm.size, dtype=np.int32))
     ref = oracle.route_layout(ex["counts"].cpu().numpy(), ex["offsets"].cpu().numpy(), perm, tile=1)
     assert np.array_equal(inv, ref["inv_perm"])
+
+
+WITH_LAYOUT_CASES = {
+    "decode8_local": (lambda: gen.cfg1(8), 0),
+    "prefill1001_global": (lambda: gen.cfg3(1001), 0),
+    "prefill1001_local": (lambda: gen.cfg3(1001, off=784, cnt=112), 0),
+    "prefill1001_local_exact": (lambda: gen.cfg3(1001, off=784, cnt=112), 3),
+    "prefill40000_global": (lambda: gen.cfg3(40000), 0),
+    "prefill65536_local": (lambda: gen.cfg3(65536, off=336, cnt=112), 0),
+    "ties4096_f32_local": (lambda: gen.cfg4(dtype="f32", off=336, cnt=112), 0),
+}
+
+
+@pytest.mark.parametrize("tile", [1, 64, 128])
+@pytest.mark.parametrize("case", sorted(WITH_LAYOUT_CASES))
+def test_route_with_layout(mr, case, tile):
+    """moe_route_with_layout: the same routing, and the layout that moe_route_layout builds
+    from it (the bf16 prefill kernel writes the layout itself; the other paths run the
+    layout kernel after routing), equal to the oracle's layout of the routing's arrays."""
+    make, path = WITH_LAYOUT_CASES[case]
+    cfg = make()
+    prev = mr.set_path(path)
+    try:
+        ref = routed(mr, cfg)
+        dev = torch.device("cuda")
+        lg = torch.from_numpy(np.ascontiguousarray(cfg["logits"]).view(
+            np.int16 if cfg["dtype"] == "bf16" else np.float32)).to(dev)
+        if cfg["dtype"] == "bf16":
+            lg = lg.view(torch.bfloat16)
+        bias = torch.from_numpy(cfg["bias"]).to(dev)
+        got = mr.route(lg, bias, k=cfg["k"], n_group=cfg["G"], topk_group=cfg["Kg"], scale=cfg["scale"],
+                       local_offset=cfg["off"], local_count=cfg["cnt"], layout_tile=tile)
+        torch.cuda.synchronize()
+    finally:
+        mr.set_path(prev)
+    assert mr.device_status() == 0
+    for key in ("packed", "counts", "offsets", "perm"):
+        assert torch.equal(got[key], ref[key]), key
+    counts, offsets, perm = (ref[k].cpu().numpy() for k in ("counts", "offsets", "perm"))
+    want = oracle.route_layout(counts, offsets, perm, tile, capacity=got["padded_rows"].numel())
+    for key in ("padded_offsets", "padded_rows", "m_indices"):
+        g = got[key].cpu().numpy()
+        assert np.array_equal(g, want[key]), (key, np.nonzero(g != want[key])[0][:8])
