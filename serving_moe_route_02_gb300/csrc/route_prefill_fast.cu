@@ -136,7 +136,8 @@ int fast_prefill_warps() { return FastSmem::NW; }
 // each row (a.logits, 16-byte aligned: each warp's rows come in one bulk copy) instead of
 // routing; an id >= NE, and every occurrence of an id that appears twice in its row, is
 // reported (kErrBadId) and left out of every output.
-template <bool INDEX>
+// LAYOUT: phase 3 also writes the expert-GEMM layout (a.poffs, a.prows, a.midx).
+template <bool INDEX, bool LAYOUT>
 __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
     k_route_prefill_fast(RouteArgs a, PrefillWS pw) {
   using L = FastSmem;
@@ -419,9 +420,8 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   }
   // the expert-GEMM layout, when asked: tile-padded offsets (an exclusive scan of the
   // padded bin sizes, in the routing scratch after the offsets)
-  const bool lay = a.poffs || a.prows || a.midx;
   int* poff_s = off_s + kFastBins + 1;
-  if (lay) {
+  if constexpr (LAYOUT) {
     for (int e = tid; e < a.NE; e += NT) poff_s[e] = (hist_s[e] + a.tile - 1) / a.tile * a.tile;
     __syncthreads();
     block_scan_fast(poff_s, poff_s, a.NE, tmp);
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
   for (int e = tid; e < a.NE; e += NT) gbase_s[e] += off_s[e] - lbase_s[e];
   __syncthreads();
   const int nvalid = lbase_s[a.NE];
-  if (!lay) {
+  if constexpr (!LAYOUT) {
 #pragma unroll 4
     for (int i = tid; i < nvalid; i += NT) a.perm[gbase_s[sbin[i]] + i] = sval[i];
   } else {
@@ -474,13 +474,16 @@ __global__ void __launch_bounds__(FastSmem::NW * 32, 1)
 }
 
 cudaError_t setup_prefill_fast(int* blocks_per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(k_route_prefill_fast<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       FastSmem::total);
+  cudaError_t e = cudaFuncSetAttribute(k_route_prefill_fast<true, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, FastSmem::total);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_route_prefill_fast<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(k_route_prefill_fast<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            FastSmem::total);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_route_prefill_fast<false>,
+  e = cudaFuncSetAttribute(k_route_prefill_fast<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           FastSmem::total);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_route_prefill_fast<false, false>,
                                                        FastSmem::NW * 32, FastSmem::total);
 }
 
@@ -508,8 +511,9 @@ cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, i
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return index ? cudaLaunchKernelEx(&cfg, k_route_prefill_fast<true>, a, ws)
-               : cudaLaunchKernelEx(&cfg, k_route_prefill_fast<false>, a, ws);
+  if (index) return cudaLaunchKernelEx(&cfg, k_route_prefill_fast<true, false>, a, ws);
+  if (a.poffs || a.prows || a.midx) return cudaLaunchKernelEx(&cfg, k_route_prefill_fast<false, true>, a, ws);
+  return cudaLaunchKernelEx(&cfg, k_route_prefill_fast<false, false>, a, ws);
 }
 
 // ------------------------------------------------------------ approximation error
