@@ -62,3 +62,26 @@ def test_missing_library_fails_loudly(tmp_path):
     import serving_moe_route_02_gb300 as mr
     with pytest.raises(ImportError):
         mr.load(str(tmp_path / "nope.so"))
+
+
+def test_route_with_layout_checks_arguments_on_the_host(libpath):
+    """moe_route_with_layout rejects a bad tile or a capacity below the bound before it
+    touches the device (no GPU here: only the host-side checks run)."""
+    import serving_moe_route_02_gb300 as mr
+    lib = mr.load()
+    T, E, k = 128, 896, 16
+    NE = mr.bins(E, k, 0)
+    need = mr.padded_capacity(T, k, NE, 128)
+    assert need >= T * k
+    dummy = ctypes.c_void_p(16)  # never dereferenced: the calls return before any launch
+
+    def call(tile, capacity, rows=True, T=T):
+        return lib.moe_route_with_layout(dummy, 1, dummy, T, E, k, 8, 4, 2.5, 0, 0, dummy, dummy, dummy,
+                                         dummy, None, None, tile, dummy, dummy if rows else None, None,
+                                         capacity, None)
+
+    assert call(0, need) == mr.E_INVALID_ARG
+    assert call(128, need - 1) == mr.E_INVALID_ARG
+    assert call(-5, need, rows=False) == mr.E_INVALID_ARG
+    assert lib.moe_route_with_layout(dummy, 1, dummy, T, E, k, 8, 9, 2.5, 0, 0, dummy, dummy, dummy,
+                                     dummy, None, None, 128, dummy, dummy, None, need, None) == mr.E_INVALID_ARG
