@@ -6,8 +6,9 @@
 // whose index depends on the data, so a warp's 32 lookups fall on shared-memory banks
 // unevenly (about 3.5-way conflicts); for all 896 experts of a row that is the costliest
 // part of routing.  Here every expert first gets a cheap approximate score, and the exact
-// table is read only for the experts a decision depends on (about 18 of 896 per row), or
-// for a whole row in the rare cases listed below.
+// table is read only for the experts a decision depends on: the survivors of the top-k
+// step (about 18 of 896 per row) and, when the group choice is uncertain, the few
+// candidates for each group's top two.
 //
 // Layout.  Lane h of a half (h = lane & 15) owns the 56 experts [56 h, 56 h + 56) as two
 // "chains" of 28: chain a = [56 h, 56 h + 28) and chain b = [56 h + 28, 56 h + 56), each a
@@ -15,7 +16,8 @@
 // as packed f16 pairs: word j holds element j of chain a (low half) and of chain b (high
 // half), so one packed max/min step tracks the two largest values of both chains at once.
 //
-// Approximate scores:
+// Approximate scores (the halving and the fma on f32 pairs, which round like the scalar
+// forms):
 //   b'' = f16(fma(0.5, tanh.approx(x / 2), c'')),  c'' = bias + (0.5 - o),
 // where o centres the values (|b''| <= R = (bias_max - bias_min + 1) / 2), so the f16
 // rounding error is at most half an f16 ulp at R.  With the offset added back, b'' + o is
@@ -28,8 +30,9 @@
 // delta = 2 eps + (2 + 2B) 2^-22 of the exact one.
 // Steps per row (everything in the row's half-warp):
 //   group choice: the 4th and 5th approximate group scores differ by more than 2 delta,
-//     so the kept set is certain; otherwise (about one row in 100) the exact group scores
-//     are computed from the table;
+//     so the kept set is certain; otherwise (about one row in 80) the group scores are
+//     computed exactly, from the table values of the experts that can be among each
+//     group's top two (b'' at least the group's approximate second largest less 2 eps);
 //   top-k: p16 = the 16th largest of the 32 kept chains' top-2 values (a bitonic sort of
 //     packed f16 pairs across the half).  At least 16 kept experts have b'' >= p16, so the
 //     exact 16th largest tau satisfies tau >= p16 + o - eps, and every kept expert whose
