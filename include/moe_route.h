@@ -39,12 +39,14 @@
  *     zeroing is needed.
  *   - Calls on one device share one workspace: calls must be ordered on the GPU
  *     (same stream, or otherwise serialised); concurrent calls race.
- *   - Routing of T <= 64 rows (and the routing behind moe_router_gemm_route) runs as
- *     one kernel launched with programmatic stream serialization that signals its
- *     dependents as it starts.  A kernel launched after it on the same stream WITH that
- *     attribute may therefore start early and must execute griddepcontrol.wait
- *     (cudaGridDependencySynchronize) before it reads the outputs; kernels launched
- *     without it, and copies, start after the routing has completed, as usual.
+ *   - Routing of T <= 64 rows, the routing behind moe_router_gemm_route, and the
+ *     bf16 routing of more rows for k = 16 and topk_group = 4 (also moe_route_index for
+ *     k = 16) run as kernels launched with programmatic stream serialization that signal
+ *     their dependents as they start.  A kernel launched after one on the same stream
+ *     WITH that attribute may therefore start early and must execute
+ *     griddepcontrol.wait (cudaGridDependencySynchronize) before it reads the outputs;
+ *     kernels launched without it, and copies, start after the routing has completed,
+ *     as usual.
  *   - Return value: MOE_ROUTE_OK or a negative moe_route_status.  A call that returns
  *     an error has enqueued nothing.  Errors detected on the device (a bounded wait
  *     that ran out) are reported by moe_route_device_status().
