@@ -377,7 +377,10 @@ int moe_router_gemm_route(const uint16_t* hidden, const uint16_t* w_router, cons
   a.cnt = local_count;
   a.NE = bins(E, k, local_count);
   a.scale = scale;
-  return launch_route_decode(a, DT_SCORE, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
+  // the routing's cluster launches while the contraction's 7 clusters of up to 16 CTAs
+  // hold their SMs; a cluster of more than 8 CTAs found no room beside them and started
+  // only as they left (about 2 us later at 32 rows)
+  return launch_route_decode(a, DT_SCORE, st, 8) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }
 
 int moe_route_index(const int32_t* packed, int T, int k, int NE, int32_t* counts,

@@ -39,8 +39,10 @@ cudaError_t launch_sigmoid_table(float* tab, float2* etab, cudaStream_t st);
 cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const float2* etab, float* s,
                            int n, cudaStream_t st);
 cudaError_t setup_decode_kernels();
-cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st);
+// max_ctas > 0 caps the cluster below the default (16 where the GPU schedules it, else 8)
+cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st, int max_ctas = 0);
 int decode_ctas(int T);  // CTAs (one cluster) of a decode launch of T <= 64 rows
+int decode_ctas(int T, int max_ctas);  // the same with at most max_ctas CTAs
 cudaError_t launch_empty(int ctas, cudaStream_t st);
 cudaError_t setup_router_gemm();
 int router_gemm_cluster();

@@ -350,11 +350,13 @@ cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const flo
 // 0.3 us); above that, the fewest CTAs that hold max(2, ceil(T / M)) rows each, M = 16
 // where clusters of 16 can be scheduled, else 8 (8 rows: 4 CTAs of 2; 64 rows: 16 CTAs
 // of 4, or 8 of 8).  Measured crossover: 6 rows.
-int decode_ctas(int T) {
+int decode_ctas(int T, int max_ctas) {
   if (T <= 5) return 1;
-  const int per = max(2, (T + g_decode_max_ctas - 1) / g_decode_max_ctas);
+  const int per = max(2, (T + max_ctas - 1) / max_ctas);
   return (T + per - 1) / per;
 }
+
+int decode_ctas(int T) { return decode_ctas(T, g_decode_max_ctas); }
 
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_empty() {}
 
@@ -438,9 +440,9 @@ static cudaError_t launch_decode_t(cudaLaunchConfig_t& cfg, const RouteArgs& a) 
   return cudaLaunchKernelEx(&cfg, k_route_decode<DT, SPEC>, a);
 }
 
-cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st) {
+cudaError_t launch_route_decode(const RouteArgs& a, int dtype, cudaStream_t st, int max_ctas) {
   if (a.T > kDecodeMaxRows) return cudaErrorInvalidValue;
-  const int ctas = decode_ctas(a.T);
+  const int ctas = decode_ctas(a.T, max_ctas > 0 && max_ctas < g_decode_max_ctas ? max_ctas : g_decode_max_ctas);
   // a CTA's row buffer and warps hold at most kDecodeRowsPerCta rows
   if (ctas < 1 || (a.T + ctas - 1) / ctas > kDecodeRowsPerCta) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
