@@ -57,6 +57,32 @@ def test_router_gemm_route(mr, weight, T, off, cnt):
     parity.compare(g, o, rcfg, exact=True)
 
 
+@pytest.mark.parametrize("H", [1024, 2048, 14336, 21504])
+def test_router_gemm_hidden_sizes(mr, H):
+    """Hidden sizes other than 7168: one 64-column block per CTA (1024), a ring of two
+    stages (2048), and K slices longer than the ring, refilled once (14336) and twice
+    (21504) as the MMAs free its stages; row counts that are not multiples of 4 or 16."""
+    cfg0 = gen.cfg2(1, H=H)
+    w_dev = torch.from_numpy(cfg0["w"].view(np.int16)).cuda()
+    for T in (1, 17, 64):
+        cfg = gen.cfg2(T, H=H)
+        hid = torch.from_numpy(cfg["hidden"].view(np.int16)).cuda()
+        bias = torch.from_numpy(cfg["bias"]).cuda()
+        out = mr.router_gemm_route(hid, w_dev, bias, want_ids=True)
+        torch.cuda.synchronize()
+        assert mr.device_status() == 0
+        logits = out["logits"].cpu().numpy()
+        ref = oracle.router_gemm(cfg["hidden"], cfg0["w"])
+        rel = logits_close(logits, ref)
+        print(f"H={H} T={T} max relative logit error {rel:.2e}")
+        assert rel <= 1e-3
+        rcfg = dict(logits=logits, dtype="f32", bias=cfg["bias"], T=T, E=896, k=16, G=8, Kg=4,
+                    scale=2.5, off=0, cnt=0)
+        o = oracle.route_cfg(rcfg)
+        g = {k: v.cpu().numpy() for k, v in out.items() if v is not None and k != "logits"}
+        parity.compare(g, o, rcfg, exact=True)
+
+
 def test_router_gemm_without_logits_out(mr, weight):
     w_np, w_dev = weight
     cfg = gen.cfg2(16)
