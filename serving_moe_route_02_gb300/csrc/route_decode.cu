@@ -3,18 +3,20 @@
 //
 // Decode rows are few (8-64 per step), so the kernel is latency-bound: CTAs of 8 warps
 // holding up to 8 rows each (one CTA up to 5 rows, then 2..4 rows per CTA over up to 16
-// CTAs; see decode_ctas), all in one cluster.  Each warp routes one row (the
-// prior art on the pages, FlashInfer's routingIndicesClusterKernel for
-// Tier<896, 16>, also ran decode routing as one cluster -- sglang PR #37).  The
-// histogram, scan and stable permutation need every row's ids.  After routing, each
-// warp stores its row's relabelled ids into an id array in every CTA of the cluster
-// (vector stores through distributed shared memory); after one cluster barrier every
-// CTA holds all rows' ids and builds, in its own shared memory, a mask of the rows
-// holding each id (two 32-bit words per id).  Counts are the masks' popcounts, a block
-// scan gives offsets, and since ids are unique within a row the stable rank of (t, j)
-// is the number of earlier rows in its id's mask.  Each CTA writes the permutation
-// entries of its own rows.  No global workspace, no atomics in global memory, no spin
-// waits.
+// CTAs, or up to 8 rows per CTA over 8 CTAs after the router contraction; see
+// decode_ctas), all in one cluster.  Each warp routes one row (the prior art on the
+// pages, FlashInfer's routingIndicesClusterKernel for Tier<896, 16>, also ran decode
+// routing as one cluster -- sglang PR #37).  The histogram, scan and stable
+// permutation need every row's ids.  After routing, each warp sends its row's
+// relabelled ids into the id array of every other CTA of the cluster (one bulk copy
+// per destination, from one lane each, through distributed shared memory, completion
+// counted in bytes on the destination's mbarrier); once its mbarrier completes a CTA
+// holds all rows' ids and builds, in its own shared memory, a mask of the rows holding
+// each id (two 32-bit words per id).  Counts are the masks' popcounts, a block scan
+// gives offsets, and since ids are unique within a row the stable rank of (t, j) is
+// the number of earlier rows in its id's mask.  Each CTA writes the permutation
+// entries of its own rows.  No global workspace and no atomics in global memory; every
+// wait is bounded.
 #include <cooperative_groups.h>
 
 #include "launch.h"
@@ -178,6 +180,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   int* offs_s = reinterpret_cast<int*>(smem + L::o_offs);
   unsigned long long* mask_s = reinterpret_cast<unsigned long long*>(smem + L::o_mask);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + L::o_mbar);
+  uint64_t* xbar = mbar + 1;  // the other CTAs' rows of ids (bulk copies, counted in bytes)
 
   int32_t* lid_all = reinterpret_cast<int32_t*>(smem + L::o_lid);
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -195,9 +198,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   // start now: before its own griddepcontrol.wait it only loads the constant score
   // table, and that wait returns once this grid has completed and its writes are visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // bytes of one row of ids as copied between CTAs (whole 16-byte chunks of the row slot)
+  const uint32_t idrow = uint32_t((a.k + 3) / 4) * 16u;
   if (tid == 0) {
     mbar_init(mbar, 1);
+    mbar_init(xbar, 1);
     fence_mbar_init();
+    // every row that another CTA routes arrives here once
+    if (nctas > 1) mbar_expect_tx(xbar, uint32_t(a.T - nrows) * idrow);
   }
   __syncthreads();
   if (tid == 0 && have) {
@@ -256,29 +264,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     }
   }
   if (nctas > 1) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  // ---- a9..a11: this warp's row of ids goes to every other CTA, 16 bytes per store
-  if (w < nrows) {
+  // ---- a9..a11: this warp's row of ids goes to every other CTA: lane c sends one bulk
+  // copy into CTA c's id array, counted on that CTA's xbar (a cluster barrier after
+  // remote stores cost more than these copies' round trip)
+  if (nctas > 1 && w < nrows) {
+    fence_proxy_async_smem();  // the row's ids (written above) visible to the copy engine
     __syncwarp();
-    const int t = row0 + w;
-    const int nch = (a.k + 3) / 4;
-    const uint32_t src = smem_addr(lid_all + t * kMaxK);
-    for (int p = lane; p < nctas * nch; p += 32) {
-      const int c = p / nch, q = p - c * nch;
-      if (c == crank) continue;
-      uint4 v;
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                   : "r"(src + 16u * q));
-      uint32_t dst;
-      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(src + 16u * q), "r"(c));
-      asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x),
-                   "r"(v.y), "r"(v.z), "r"(v.w)
-                   : "memory");
+    const uint32_t src = smem_addr(lid_all + (row0 + w) * kMaxK);
+    if (lane < nctas && lane != crank) {
+      uint32_t dst, bar;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(dst) : "r"(src), "r"(lane));
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(bar) : "r"(smem_addr(xbar)), "r"(lane));
+      asm volatile(
+          "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+          "[%3];" ::"r"(dst),
+          "r"(src), "r"(idrow), "r"(bar)
+          : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
   }
-  // release the stores above, acquire every other CTA's (one CTA: a block barrier)
-  if (nctas > 1) cluster.sync();
-  else __syncthreads();
+  // this CTA's own rows (block barrier), then every other CTA's (their copies)
+  __syncthreads();
+  if (nctas > 1 && !mbar_wait_bounded(xbar, 0, a.err)) {
+    // a copy into this CTA may still be on its way: every CTA sends its rows once its
+    // own bounded row wait is over; wait that long again before going on
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(xbar, 0) && globaltimer_ns() - t0 < 2 * kWaitLimitNs) {
+    }
+  }
   uint32_t* mask32 = reinterpret_cast<uint32_t*>(mask_s);
   const int kk = SPEC ? 16 : a.k;
   for (int x = tid; x < a.T * kk; x += kDecodeThreads) {
@@ -302,6 +315,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     a.perm[pos] = t * a.k + lane;
     if (a.inv) a.inv[t * a.k + lane] = pos;
   }
+  // the outgoing copies have read this CTA's id rows before it leaves
+  if (nctas > 1 && w < nrows && lane < nctas && lane != crank)
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // --------------------------------------------------------------- sigmoid table
