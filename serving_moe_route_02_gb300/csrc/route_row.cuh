@@ -259,14 +259,17 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
 #pragma unroll
     for (int i = 0; i < kEPL; ++i) smask |= (b[i] >= tau0) ? (1u << i) : 0u;
   }
+  // inclusive prefix of the per-lane counts c (0..28, five bits) by bit slices: five
+  // independent ballots instead of a five-step shuffle chain
   const int c = __popc(smask);
-  int incl = c;
+  const uint32_t le = 0xffffffffu >> (31 - lane);  // lanes 0..lane
+  int incl = 0, total = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(FULL, incl, o);
-    if (lane >= o) incl += n;
+  for (int bit = 0; bit < 5; ++bit) {
+    const uint32_t bal = __ballot_sync(FULL, (c >> bit) & 1);
+    incl += __popc(bal & le) << bit;
+    total += __popc(bal) << bit;
   }
-  const int total = __shfl_sync(FULL, incl, 31);
   __syncwarp();  // ws.b visible to the warp
 
   // composite 32-bit keys (b, position) need tau0 > 0 and survivors within 2^26 float
