@@ -174,7 +174,10 @@ int moe_route_quant(const void* logits, int logits_dtype, const float* bias, int
  *               expert e), 16-byte aligned.  H % 64 == 0.
  *   1 <= T <= 64 (decode batches).
  *   logits_out  [T, E] float32 out, nullable (the fp32 logits the routing used).
- *   other arguments as moe_route.  Supported: E = 896, n_group = 8, H % 64 == 0.
+ *   other arguments as moe_route.  Supported: E = 896, n_group = 8, and H / 64 a
+ *   multiple of the contraction's cluster size (16 K-splits where the GPU schedules
+ *   seven clusters of 16 CTAs, as a GB300 does, else 8): H a multiple of 1024 on a
+ *   GB300.  Other H return MOE_ROUTE_E_UNSUPPORTED.
  * w_router is read as a constant model weight: the contraction kernel is launched as a
  * programmatic dependent and starts loading the weight before the preceding kernel on
  * `stream` has completed (hidden, bias and all outputs wait for it).  The weight must
