@@ -102,6 +102,14 @@ def test_router_gemm_rejects(mr, weight):
     with pytest.raises(mr.MoeRouteError) as e:
         mr.router_gemm_route(hid, w_dev, bias)
     assert e.value.status == mr.E_UNSUPPORTED
+    # H / 64 = 15 blocks: not a multiple of the K-split count (16, or 8)
+    hid = torch.zeros((8, 960), dtype=torch.int16, device="cuda")
+    w = torch.zeros((896, 960), dtype=torch.int16, device="cuda")
+    with pytest.raises(mr.MoeRouteError) as e:
+        mr.router_gemm_route(hid, w, bias)
+    assert e.value.status == mr.E_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert mr.device_status() == 0
 
 
 def test_router_gemm_repeated_and_replayed(mr, weight):
