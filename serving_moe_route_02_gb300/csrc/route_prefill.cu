@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         const int l = lid_of(c0, r);
         bool use = true;
         if constexpr (L::INDEX) {
-          // kept ids carry phase 1's verdict; staged ones are checked again
+          // kept ids carry phase 1's decision; staged ones are checked again
           // (keep is the same in every lane: either all lanes of kmask shuffle or none)
           const bool rep = keep ? false : repeated_in_row(l, kmask, a.k);
           use = l < a.NE && !rep;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(PrefillSmem<DT, SPEC>::NW * 32, 1)
         const int l = lid_of(c0, r);
         bool use = true;
         if constexpr (L::INDEX) {
-          // kept ids carry phase 1's verdict; staged ones are checked again
+          // kept ids carry phase 1's decision; staged ones are checked again
           // (keep is the same in every lane: either all lanes of kmask shuffle or none)
           const bool rep = keep ? false : repeated_in_row(l, kmask, a.k);
           use = l < a.NE && !rep;
