@@ -155,7 +155,8 @@ int moe_route_with_layout(const void* logits, int logits_dtype, const float* bia
  *   Routing arguments and outputs are those of moe_route (same results).
  * Errors: those of moe_route; INVALID_ARG for H <= 0, H % 32 != 0, NULL x / x_q /
  * x_scales with T > 0, or misaligned x / x_q; UNSUPPORTED for T > 64.  One kernel launch
- * (a programmatic dependent, like moe_route for T <= 64 rows).
+ * (a programmatic dependent, like moe_route for T <= 64 rows): its first thread-block
+ * cluster routes, the clusters after it quantise.
  */
 #define MOE_ROUTE_QUANT_MAX_TOKENS 64
 int moe_route_quant(const void* logits, int logits_dtype, const float* bias, int T, int E, int k,

@@ -198,6 +198,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
   // start now: before its own griddepcontrol.wait it only loads the constant score
   // table, and that wait returns once this grid has completed and its writes are visible
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if constexpr (QUANT) {
+    // the activations' quantisation runs on the clusters after the first one, so that it
+    // shares no SM with the routing; every warp of those CTAs takes a share
+    if (blockIdx.x >= unsigned(nctas)) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // x is an input
+      mxfp4_quant_blocks(a, (int(blockIdx.x) - nctas) * kDecodeRowsPerCta + w,
+                         (int(gridDim.x) - nctas) * kDecodeRowsPerCta);
+      return;
+    }
+  }
   // bytes of one row of ids as copied between CTAs (whole 16-byte chunks of the row slot)
   const uint32_t idrow = uint32_t((a.k + 3) / 4) * 16u;
   if (tid == 0) {
@@ -227,16 +237,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
              uint32_t(nrows) * L::ROWB, mbar);
   }
-  // the activations' quantisation: by the warps that route no row (warps rpc.. of every
-  // CTA), while the others route; by all warps, ahead of the row wait, if none is free
-  bool quant_warp = false;
-  if constexpr (QUANT) {
-    const int qw = kDecodeRowsPerCta - rpc;
-    quant_warp = qw > 0 && w >= rpc;
-    if (qw <= 0) mxfp4_quant_blocks(a, crank * kDecodeRowsPerCta + w, nctas * kDecodeRowsPerCta);
-    else if (quant_warp) mxfp4_quant_blocks(a, crank * qw + (w - rpc), nctas * qw);
-  }
-  if (have && !quant_warp) mbar_wait_bounded(mbar, 0, a.err);
+  if (have) mbar_wait_bounded(mbar, 0, a.err);
 
   SlotOut o = {};
   if constexpr (DT == DT_PACKED) {
@@ -451,7 +452,16 @@ template <int DT, bool SPEC>
 static cudaError_t launch_decode_t(cudaLaunchConfig_t& cfg, const RouteArgs& a) {
   cfg.dynamicSmemBytes = DecodeSmem<DT>::total;
   if constexpr (DT == DT_BF16 || DT == DT_F32) {
-    if (a.qx != nullptr) return cudaLaunchKernelEx(&cfg, k_route_decode<DT, SPEC, true>, a);
+    if (a.qx != nullptr) {
+      // route+quant: the routing cluster, then as many clusters of the same size as give
+      // every quantising warp at most one pass of kQSteps steps (8 blocks a step)
+      const int ctas = int(cfg.gridDim.x);
+      const long long steps = (static_cast<long long>(a.T) * (a.qH >> 5) + 7) / 8;
+      const long long per_cluster = static_cast<long long>(ctas) * kDecodeRowsPerCta * kQSteps;
+      const long long q = steps > 0 ? (steps + per_cluster - 1) / per_cluster : 0;
+      cfg.gridDim.x = unsigned(ctas * (1 + q));
+      return cudaLaunchKernelEx(&cfg, k_route_decode<DT, SPEC, true>, a);
+    }
   }
   return cudaLaunchKernelEx(&cfg, k_route_decode<DT, SPEC>, a);
 }
