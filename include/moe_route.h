@@ -414,7 +414,7 @@ int moe_route_host_release(void);
  */
 int moe_route_empty(int ctas, struct CUstream_st* stream);
 
-/* CTAs (one thread-block cluster) of the routing kernel for T <= 64 rows: 1 for T <= 5;
+/* CTAs (one thread-block cluster) of the routing kernel for T <= 64 rows: 1 for T <= 4;
  * otherwise the fewest that hold max(2, ceil(T / M)) rows each, M = 16 where the GPU can
  * schedule clusters of 16 CTAs (else 8).  Creates the device state like
  * moe_route_reserve.  INVALID_ARG for T outside [0, 64]. */

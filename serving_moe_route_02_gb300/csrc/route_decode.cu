@@ -2,7 +2,7 @@
 // cluster, plus the sigmoid table and elementwise score kernels.
 //
 // Decode rows are few (8-64 per step), so the kernel is latency-bound: CTAs of 8 warps
-// holding up to 8 rows each (one CTA up to 5 rows, then 2..4 rows per CTA over up to 16
+// holding up to 8 rows each (one CTA up to 4 rows, then 2..4 rows per CTA over up to 16
 // CTAs, or up to 8 rows per CTA over 8 CTAs after the router contraction; see
 // decode_ctas), all in one cluster.  Each warp routes one row (the prior art on the
 // pages, FlashInfer's routingIndicesClusterKernel for Tier<896, 16>, also ran decode
@@ -368,7 +368,7 @@ cudaError_t launch_sigmoid(const void* x, int dtype, const float* tab, const flo
 // where clusters of 16 can be scheduled, else 8 (8 rows: 4 CTAs of 2; 64 rows: 16 CTAs
 // of 4, or 8 of 8).  Measured crossover: 6 rows.
 int decode_ctas(int T, int max_ctas) {
-  if (T <= 5) return 1;
+  if (T <= 4) return 1;
   const int per = max(2, (T + max_ctas - 1) / max_ctas);
   return (T + per - 1) / per;
 }
