@@ -237,7 +237,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_route_decode(RouteArgs a)
     bulk_g2s(rows, static_cast<const uint8_t*>(a.logits) + size_t(row0) * L::ROWB,
              uint32_t(nrows) * L::ROWB, mbar);
   }
-  if (have) mbar_wait_bounded(mbar, 0, a.err);
+  // only the routing warps need the rows; the others go on to the hardware barriers below
+  // instead of polling this one
+  if (have && w < nrows) mbar_wait_bounded(mbar, 0, a.err);
 
   SlotOut o = {};
   if constexpr (DT == DT_PACKED) {
