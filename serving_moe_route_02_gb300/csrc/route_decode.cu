@@ -47,7 +47,11 @@ struct DecodeSmem {
   static constexpr int o_mask = align_up(o_offs + (kMaxBins + 1) * 4, 128);
   static constexpr int o_tmp = align_up(o_mask + kMaxBins * 8, 128);
   static constexpr int o_mbar = align_up(o_tmp + 32 * 4, 128);
-  static constexpr int total = o_mbar + 64;
+  static constexpr int used = o_mbar + 64;
+  // at least 118 KB, more than half an SM's shared memory, so that the CTAs of the next
+  // call (a programmatic dependent, launched early) never share an SM with this one's
+  // (16 rows: 3.37 -> 3.29 us per call)
+  static constexpr int total = used > 118 * 1024 ? used : 118 * 1024;
 };
 
 static_assert(DecodeSmem<DT_F32>::total <= 227 * 1024, "decode smem (f32) exceeds 227 KB");
