@@ -70,6 +70,16 @@ def test_route_quant_f32_logits_other_width(mr):
     check(mr, cfg, gen.mx_activations(8, H=4096, kind="ties"))
 
 
+@pytest.mark.parametrize("T,H", [(64, 32), (64, 21504), (3, 28672)])
+def test_route_quant_quantising_clusters(mr, T, H):
+    """The quantisation runs on the clusters after the routing cluster, as many as give
+    every quantising warp at most one pass: one quantising cluster with a single short
+    step in all (64 rows of 32), three quantising clusters of 16 CTAs (64 rows of
+    21,504), three one-CTA quantising clusters beside a one-CTA routing cluster (3 rows
+    of 28,672)."""
+    check(mr, gen.cfg1(T), gen.mx_activations(T, H=H))
+
+
 def test_route_quant_empty_and_errors(mr):
     lib = mr.load()
     cfg = gen.cfg1(8)
