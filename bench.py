@@ -423,9 +423,9 @@ def index_timing(torch, mr, dev, out, reps=20, replays=10):
 
 
 def run_case(torch, mr, dev, args, T=64):
-    """Plain launches of one path, for ncu captures: decode routing or contraction +
-    routing at 64 rows, or the expert-GEMM layout / the index of packed ids at 65,536
-    rows (global ids, tile 128)."""
+    """Plain launches of one path, for ncu captures: decode routing, route+quant (H =
+    7168) or contraction + routing at 64 rows, or the expert-GEMM layout / the index of
+    packed ids at 65,536 rows (global ids, tile 128)."""
     if args.case in ("layout", "index"):
         cfg = gen.cfg3(T_PREFILL)
         lg = to_dev_bf16(torch, cfg["logits"], dev)
@@ -438,12 +438,17 @@ def run_case(torch, mr, dev, args, T=64):
             idx = mr.route_index(out["packed"], E)
             step = lambda: mr.route_index(out["packed"], E, out=idx)  # noqa: E731
         T = T_PREFILL
-    elif args.case == "decode":
+    elif args.case in ("decode", "quant"):
         cfg = gen.cfg1(T)
         lg = to_dev_bf16(torch, cfg["logits"], dev)
         bias = torch.from_numpy(cfg["bias"]).to(dev)
         out = mr.alloc_outputs(T, E, K, 112, dev)
-        step = lambda: mr.route(lg, bias, local_offset=336, local_count=112, out=out)  # noqa: E731
+        if args.case == "decode":
+            step = lambda: mr.route(lg, bias, local_offset=336, local_count=112, out=out)  # noqa: E731
+        else:
+            x = to_dev_bf16(torch, gen.mx_activations(T), dev)
+            step = lambda: mr.route_quant(lg, bias, x, local_offset=336, local_count=112,  # noqa: E731
+                                          out=out)
     else:
         cfg = gen.cfg2(T)
         w = torch.from_numpy(cfg["w"].view(np.int16)).to(dev)
@@ -477,9 +482,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--case", default=None, choices=["decode", "gemm", "layout", "index"],
-                    help="run only --steps plain launches of one path (decode routing or "
-                         "contraction + routing at 64 rows, expert-GEMM layout or index of "
+    ap.add_argument("--case", default=None, choices=["decode", "quant", "gemm", "layout", "index"],
+                    help="run only --steps plain launches of one path (decode routing, "
+                         "route+quant or contraction + routing at 64 rows, expert-GEMM layout or index of "
                          "packed ids at 65,536 rows) and print a one-line summary: the "
                          "commands profiled under ncu")
     ap.add_argument("--quick", action="store_true",
