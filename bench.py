@@ -9,9 +9,12 @@ the stable permutation (one kernel launch).  value = routed tokens/s over all ra
 
 Also reported (same JSON line): decode routing latency at 8-64 rows (rank-local ids,
 CUDA-graph replay) against an empty-kernel floor replayed the same way, the router
-contraction + routing at 1-64 rows, the expert-GEMM layout at 65,536 rows, a roofline
-object for the prefill kernel, the CPU oracle's throughput on the machine's host, an
-end-to-end number with host buffers, and SM clocks sampled during the timed region.
+contraction + routing at 1-64 rows, the expert-GEMM layout at 65,536 rows, a table of the
+other routing configurations (8-row fp32 decode; prefill at 16,384 and 65,536 rows and the
+tie-heavy 4,096-row batch, global and rank-local ids, cold and warm L2), a roofline object
+for the prefill kernel with its special-function-unit bound beside the HBM one, the CPU
+oracle's throughput on the machine's host, an end-to-end number with host buffers, and SM
+clocks sampled during the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 For N > 1 launch under torch.distributed.run; each rank routes its own batch (weak
@@ -422,6 +425,113 @@ def index_timing(torch, mr, dev, out, reps=20, replays=10):
             "algorithmic_bytes": T * 16 * 4 + T * 16 * 4 + 4 * (2 * NE + 1)}
 
 
+L2_BYTES = 129 * 2**20
+
+
+def _graph_us(torch, st, calls, reps, replays=5):
+    """Median µs per call of `calls` (a list of closures, run in turn) captured `reps`
+    times over into one CUDA graph and replayed on stream `st`."""
+    with torch.cuda.stream(st):
+        for c in calls:
+            c()
+        st.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            for i in range(reps):
+                calls[i % len(calls)]()
+        g.replay()
+        st.synchronize()
+        samples = []
+        for _ in range(replays):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            g.replay()
+            b.record(st)
+            b.synchronize()
+            samples.append(a.elapsed_time(b) * 1e3 / reps)
+    return statistics.median(samples)
+
+
+# tanh.approx.f32 results per clock per SM on GB300, measured by a throughput probe (8
+# independent chains per thread, all SMs busy): 15.0, against 29.8 for ex2.approx.f32
+MUFU_TANH_PER_CLK_SM = 15.0
+
+
+def mufu_bound(torch, dev, T, kernel_ms, clocks):
+    """The second bound of the prefill kernel: one tanh.approx per expert and row on the
+    special-function units (the exact table lookups are not MUFU work)."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or 2070.0
+    peak = MUFU_TANH_PER_CLK_SM * sms * mhz * 1e6
+    ops = T * E
+    floor_us = ops / peak * 1e6
+    return {"ops_per_launch": ops, "peak_ops_per_s": peak, "floor_us": round(floor_us, 2),
+            "frac": round(floor_us / (kernel_ms * 1e3), 3),
+            "peak_source": f"measured tanh.approx.f32 rate ({MUFU_TANH_PER_CLK_SM} per clock per SM) "
+                           f"x {sms} SMs x {mhz:.0f} MHz"}
+
+
+def workload_table(torch, mr, dev, bufs, bias3, peak_gbs):
+    """The measurement table of the routing configurations: small fp32 decode (8 rows),
+    prefill at 16,384 and 65,536 rows (global ids and the last rank's local ids, offset
+    784, count 112) and the tie-heavy 4,096-row batch (fp32 and bf16 logits, global and
+    local ids), each cold (as many input/output sets in turn as hold more than twice the
+    L2, so no call finds its input in L2) and warm (the same buffers every call).  Calls
+    are CUDA-graph replays of back-to-back calls; GB/s counts the algorithmic bytes (logits
+    in, packed and perm out, counts, offsets and bias)."""
+    st = torch.cuda.Stream(device=dev)
+    rows = []
+
+    def add(name, T, dtype, off, cnt, sets, reps, bias):
+        NE = mr.bins(E, K, cnt) if cnt else E
+        row_in = E * (2 if dtype == "bf16" else 4)
+        nbytes = T * (row_in + 2 * K * 4) + NE * 4 + (NE + 1) * 4 + E * 4
+        for state in ("cold", "warm"):
+            use = sets if state == "cold" else sets[:1]
+            outs = [mr.alloc_outputs(T, E, K, cnt, dev) for _ in use]
+            calls = [(lambda x=x, o=o: mr.route(x, bias, local_offset=off, local_count=cnt, out=o, stream=st))
+                     for x, o in zip(use, outs)]
+            us = _graph_us(torch, st, calls, reps if state == "warm" else max(reps, len(use)))
+            rows.append({"workload": name, "T": T, "logits": dtype,
+                         "ids": f"local {off}/{cnt}" if cnt else "global", "l2": state,
+                         "sets": len(use), "us_per_call": round(us, 3),
+                         "tokens_per_s": round(T / (us * 1e-6)), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                         "frac_of_hbm": round(nbytes / (us * 1e-6) / 1e9 / peak_gbs, 3)})
+            del outs
+    # small fp32 decode batch (8 rows, global ids): latency, with the empty-kernel floor
+    c0 = gen.cfg0(8)
+    x0 = torch.from_numpy(c0["logits"]).to(dev)
+    b0 = torch.from_numpy(c0["bias"]).to(dev)
+    o0 = mr.alloc_outputs(8, E, K, 0, dev)
+    us0 = _graph_us(torch, st, [lambda: mr.route(x0, b0, out=o0, stream=st)], 200)
+    fl0 = _graph_us(torch, st, [lambda: mr.empty_kernel(mr.decode_ctas(8), stream=st)], 200)
+    rows.append({"workload": "decode fp32 N(0,1)", "T": 8, "logits": "f32", "ids": "global", "l2": "warm",
+                 "sets": 1, "us_per_call": round(us0, 3), "floor_us": round(fl0, 3),
+                 "ratio_to_floor": round(us0 / fl0, 3)})
+    # prefill, Zipf-skewed bf16 logits: slices of the headline's rotating input sets
+    for T in (16384, T_PREFILL):
+        per = T_PREFILL // T
+        slices = [b[i * T:(i + 1) * T] for b in bufs for i in range(per)]
+        n_cold = min(len(slices), max(2, -(-2 * L2_BYTES // (T * E * 2))))
+        for off, cnt in ((0, 0), (784, 112)):
+            add("prefill bf16 N(0,1)+Zipf offsets", T, "bf16", off, cnt, slices[:n_cold],
+                20 if T == T_PREFILL else 60, bias3)
+    # tie-heavy batch: the same logits copied into enough buffers to exceed twice the L2
+    for dtype in ("f32", "bf16"):
+        c4 = gen.cfg4(4096, dtype=dtype)
+        b4 = torch.from_numpy(c4["bias"]).to(dev)
+        host = c4["logits"]
+        one = torch.from_numpy(host).to(dev) if dtype == "f32" else to_dev_bf16(torch, host, dev)
+        n_cold = max(2, -(-2 * L2_BYTES // (one.numel() * one.element_size())))
+        sets = [one] + [one.clone() for _ in range(n_cold - 1)]
+        for off, cnt in ((0, 0), (784, 112)):
+            add("ties: j/64 logits, hot 16-expert set in a quarter of rows", 4096, dtype, off, cnt, sets, 60, b4)
+        del sets
+    torch.cuda.synchronize()
+    return rows
+
+
 def run_case(torch, mr, dev, args, T=64):
     """Plain launches of one path, for ncu captures: decode routing, route+quant (H =
     7168) or contraction + routing at 64 rows, or the expert-GEMM layout / the index of
@@ -603,14 +713,16 @@ def main():
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt[0])
 
-    decode = gemm = layout = index = None
+    peaks, peak_src = measured_peaks()
+    decode = gemm = layout = index = table = None
     if rank == 0 and not (args.no_decode or args.quick):
         decode = decode_latency(torch, mr, dev)
         gemm = gemm_route_latency(torch, mr, dev)
         layout = layout_timing(torch, mr, dev, outs[0], T_PREFILL, bufs=bufs, bias=bias)
         index = index_timing(torch, mr, dev, outs[0])
+        table = workload_table(torch, mr, dev, bufs, bias, peaks["hbm_gbs"])
+        ok = ok and mr.device_status() == 0
 
-    peaks, peak_src = measured_peaks()
     ab = algorithmic_bytes(T_PREFILL)
     achieved = ab / (kernel_ms * 1e-3) / 1e9
     traffic = None
@@ -634,7 +746,8 @@ def main():
                      "kernel": "k_route_prefill_fast", "algorithmic_bytes": ab,
                      "kernel_us": kernel_ms * 1e3,
                      "kernel_us_method": "timed region / launches (one launch per step, back to back)",
-                     "peak_source": f"{peak_src} hbm_gbs (copy)"},
+                     "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "mufu": mufu_bound(torch, dev, T_PREFILL, kernel_ms, clocks)},
         "clocks": clocks,
         "e2e": ({"value": world * T_PREFILL / (e2e_ms * 1e-3), "unit": "tokens/s",
                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
@@ -652,6 +765,8 @@ def main():
         line["route_layout"] = layout
     if index is not None:
         line["route_index"] = index
+    if table is not None:
+        line["workloads"] = table
     if rank == 0 and not (args.no_cpu_baseline or args.quick):
         line["cpu_baseline"] = cpu_baseline()
     if world > 1:
