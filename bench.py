@@ -635,6 +635,23 @@ def main():
     if mr.device_status() != 0:
         raise SystemExit("device status error during warm-up")
 
+    # The K timed steps are captured once as a CUDA graph and replayed, so that the
+    # launches run back to back with no host work between them: one kernel launch per
+    # step, each a programmatic dependent of the one before (its CTAs start as the previous
+    # launch's leave).  A Python loop of calls cannot always enqueue a 55 us launch before
+    # the previous one ends; the host-side cost of a call is part of the e2e number.
+    gst = torch.cuda.Stream(device=dev)
+    gst.wait_stream(stream)
+    with torch.cuda.stream(gst):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gst):
+            for i in range(args.steps):
+                mr.route(bufs[i % NBUF], bias, out=outs[i % NBUF], stream=gst)
+        graph.replay()  # untimed: the graph's first replay
+    gst.synchronize()
+    if mr.device_status() != 0:
+        raise SystemExit("device status error in the graph's first replay")
+
     sampler = ClockSampler(gpu_uuid(torch, local))
     sampler.start()
     if world > 1:
@@ -643,19 +660,17 @@ def main():
     sampler.mark(0)
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_begin.record(stream)
-    for i in range(args.steps):
-        mr.route(bufs[i % NBUF], bias, out=outs[i % NBUF])
-    t_end.record(stream)
+    with torch.cuda.stream(gst):  # a graph replays on the current stream
+        t_begin.record(gst)
+        graph.replay()
+        t_end.record(gst)
     torch.cuda.synchronize()
     sampler.mark(1)
     if world > 1:
         dist.barrier()
     elapsed_ms = t_begin.elapsed_time(t_end)
-    # One kernel launch per step, back to back, each a programmatic dependent of the one
-    # before (its CTAs start as the previous launch's CTAs leave): the average launch
-    # duration over the timed region is the region's length over its launches.  Events
-    # recorded between the launches would cut that overlap and add their own gap.
+    # the average launch duration over the timed region: its length over its launches
+    # (events between the launches would cut their overlap and add their own gap)
     kernel_ms = elapsed_ms / args.steps
     if world > 1:
         tt = torch.tensor([elapsed_ms, kernel_ms], device=dev, dtype=torch.float64)
@@ -745,7 +760,8 @@ def main():
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": "k_route_prefill_fast", "algorithmic_bytes": ab,
                      "kernel_us": kernel_ms * 1e3,
-                     "kernel_us_method": "timed region / launches (one launch per step, back to back)",
+                     "kernel_us_method": "timed region / launches (one CUDA-graph replay of the K steps, "
+                                         "one launch per step, back to back)",
                      "peak_source": f"{peak_src} hbm_gbs (copy)",
                      "mufu": mufu_bound(torch, dev, T_PREFILL, kernel_ms, clocks)},
         "clocks": clocks,

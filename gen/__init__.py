@@ -183,7 +183,12 @@ def cfg_decision_edges(kind: str, T: int = 3000, E: int = E_KIMI, off: int = 0, 
       negative    prefill logits, bias ~U(-2.1, -1.9): every biased score is negative;
       large_bias  prefill logits, bias ~U(-50, 50);
       plateau     N(0,1) logits (seed 10) with 200 seeded experts per row (seed 11) at 4.0 and
-                  bias 0, so the k-th largest score is shared by far more than k experts.
+                  bias 0, so the k-th largest score is shared by far more than k experts;
+      band        N(0,1) logits (seed 10) with 48 seeded experts per row (seed 13), 12 in each
+                  of groups 0-3, at 3.0; the biases of groups 0-3 are distinct multiples of
+                  2^-21 (a seeded permutation, seed 14), the others' -0.5, so that about 48
+                  biased scores of a row lie within 2.2e-4 of each other: distinct, but
+                  closer than the approximate scores can tell apart.
     """
     G = G_KIMI
     gsz = E // G
@@ -208,6 +213,14 @@ def cfg_decision_edges(kind: str, T: int = 3000, E: int = E_KIMI, off: int = 0, 
         x[np.arange(T)[:, None], cols] = 4.0
         logits = f32_to_bf16_bits(x)
         bias[:] = 0.0
+    elif kind == "band":
+        x = normal_f32(10, T * E).reshape(T, E)
+        pick = (raw64(13, T * 48) % np.uint64(gsz)).astype(np.int64).reshape(T, 4, 12)
+        cols = (pick + (np.arange(4) * gsz)[None, :, None]).reshape(T, 48)
+        x[np.arange(T)[:, None], cols] = 3.0
+        logits = f32_to_bf16_bits(x)
+        bias = np.full(E, -0.5, dtype=np.float32)
+        bias[:4 * gsz] = (permutation(14, 4 * gsz).astype(np.float64) * 2.0 ** -21).astype(np.float32)
     else:
         raise ValueError(kind)
     return dict(base, logits=logits, bias=bias)

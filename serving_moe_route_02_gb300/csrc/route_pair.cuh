@@ -42,8 +42,9 @@
 //     ascending id order, looked up in the exact table (two per lane) and ranked by a
 //     bitonic sort of 32-bit keys (exact b, then id), which gives slots 0..15;
 //   weights from the exact scores in slot order, relabel, pack.
-// Rare cases: more than 32 survivors in a row, or keys that do not fit 32 bits, take an
-// exact extraction (16 rounds of a half-warp maximum over the survivors).
+// Rare cases: 33 to 64 survivors in a row are ranked the same way, four per lane in a
+// 64-key sort; more than 64, or keys that do not fit 32 bits, take an exact extraction
+// (16 rounds of a half-warp maximum over the survivors).
 #pragma once
 #include "route_row.cuh"
 
@@ -207,6 +208,36 @@ __device__ __forceinline__ void bitonic32_u32(uint32_t& k0, uint32_t& k1, int h)
         const bool keep_max = lower == desc;
         k0 = keep_max ? max(k0, p0) : min(k0, p0);
         k1 = keep_max ? max(k1, p1) : min(k1, p1);
+      }
+    }
+  }
+}
+
+// Descending bitonic sort of 64 uint32 keys held four per lane of a half-warp (lane h
+// holds positions 4 h .. 4 h + 3).
+__device__ __forceinline__ void bitonic64_u32(uint32_t (&k)[4], int h) {
+#pragma unroll
+  for (int kk = 2; kk <= 64; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j >= 1; j >>= 1) {
+      if (j >= 4) {
+        // partner in lane h ^ (j / 4), same element; direction and side depend on h only
+        const bool desc = ((4 * h) & kk) == 0;
+        const bool keep_max = (((4 * h) & j) == 0) == desc;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t p = __shfl_xor_sync(0xffffffffu, k[e], j >> 2);
+          k[e] = keep_max ? max(k[e], p) : min(k[e], p);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (e & j) continue;
+          const bool desc = ((4 * h + e) & kk) == 0;
+          const uint32_t mx = max(k[e], k[e | j]), mn = min(k[e], k[e | j]);
+          k[e] = desc ? mx : mn;
+          k[e | j] = desc ? mn : mx;
+        }
       }
     }
   }
@@ -442,42 +473,81 @@ __device__ __forceinline__ SlotOut route_pair(const void* row0, const void* row1
     }
   }
   if (slow) {
-    // exact extraction: 16 rounds, each lane offering its best remaining survivor; equal
-    // scores go to the lower lane (lower ids)
-    uint32_t ra = ma, rb = mb;
-    const uint32_t hmask = 0xFFFFu << hbase;
-    for (int j = 0; j < K; ++j) {
-      uint32_t best = 0u;
-      int bid = -1;
-      float bs = 0.0f;
-      for (uint32_t m = ra; m; m &= m - 1u) {
-        const int id = e0 + __ffs(m) - 1;
-        float si;
-        const uint32_t kq = fkey(exact(id, &si));
-        if (kq > best) {
-          best = kq;
-          bid = id;
-          bs = si;
+    if (pb.ok && !__any_sync(FULL, total > 64)) {
+      // 33 to 64 survivors (many experts within the error band of the cutoff): four per
+      // lane, their ids as 16-bit values in the id scratch, 32-bit keys (exact b relative
+      // to the cutoff, then position) in a 64-key sort; the 16 winners' scores are looked
+      // up again by the slot lanes
+      uint16_t* sid16 = reinterpret_cast<uint16_t*>(ws.sid[half]);
+      int pos = incl - cnt;
+      for (uint32_t m = ma; m; m &= m - 1u) sid16[pos++] = static_cast<uint16_t>(e0 + __ffs(m) - 1);
+      for (uint32_t m = mb; m; m &= m - 1u) sid16[pos++] = static_cast<uint16_t>(e0 + kChain + __ffs(m) - 1);
+      __syncwarp();
+      const uint32_t bb = __float_as_uint(base);
+      uint32_t kq[4];
+      bool fit = base > 0.0f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int q = 4 * h + e;
+        float se;
+        const float bx = exact(sid16[min(q, total - 1)], &se);
+        kq[e] = 0u;
+        if (q < total) {
+          fit = fit && __float_as_uint(bx) - bb < (1u << 26) - 1u;  // (range + 1) << 6 fits
+          kq[e] = ((__float_as_uint(bx) - bb + 1u) << 6) | uint32_t(63 - q);
         }
       }
-      for (uint32_t m = rb; m; m &= m - 1u) {
-        const int id = e0 + kChain + __ffs(m) - 1;
-        float si;
-        const uint32_t kq = fkey(exact(id, &si));
-        if (kq > best) {
-          best = kq;
-          bid = id;
-          bs = si;
+      if (__all_sync(FULL, fit)) {
+        bitonic64_u32(kq, h);
+        // positions 0..15 (lanes 0..3 of the half) are slots 0..15
+        if (h < 4) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ws.slot_id[half][4 * h + e] = sid16[63 - int(kq[e] & 63u)];
         }
+        __syncwarp();
+        ws.slot_s[half][h] = __ldg(stab + sig_index(row[ws.slot_id[half][h]]));
+        slow = false;
       }
-      const uint32_t top = half_max(best);
-      const uint32_t cand = __ballot_sync(FULL, best == top && bid >= 0) & hmask;
-      const int win = __ffs(cand) - 1;
-      if (lane == win) {
-        ws.slot_id[half][j] = bid;
-        ws.slot_s[half][j] = bs;
-        if (bid < e0 + kChain) ra &= ~(1u << (bid - e0));
-        else rb &= ~(1u << (bid - e0 - kChain));
+      __syncwarp();  // the id scratch is rewritten below when the keys did not fit
+    }
+    if (slow) {
+      // exact extraction: 16 rounds, each lane offering its best remaining survivor; equal
+      // scores go to the lower lane (lower ids)
+      uint32_t ra = ma, rb = mb;
+      const uint32_t hmask = 0xFFFFu << hbase;
+      for (int j = 0; j < K; ++j) {
+        uint32_t best = 0u;
+        int bid = -1;
+        float bs = 0.0f;
+        for (uint32_t m = ra; m; m &= m - 1u) {
+          const int id = e0 + __ffs(m) - 1;
+          float si;
+          const uint32_t kq = fkey(exact(id, &si));
+          if (kq > best) {
+            best = kq;
+            bid = id;
+            bs = si;
+          }
+        }
+        for (uint32_t m = rb; m; m &= m - 1u) {
+          const int id = e0 + kChain + __ffs(m) - 1;
+          float si;
+          const uint32_t kq = fkey(exact(id, &si));
+          if (kq > best) {
+            best = kq;
+            bid = id;
+            bs = si;
+          }
+        }
+        const uint32_t top = half_max(best);
+        const uint32_t cand = __ballot_sync(FULL, best == top && bid >= 0) & hmask;
+        const int win = __ffs(cand) - 1;
+        if (lane == win) {
+          ws.slot_id[half][j] = bid;
+          ws.slot_s[half][j] = bs;
+          if (bid < e0 + kChain) ra &= ~(1u << (bid - e0));
+          else rb &= ~(1u << (bid - e0 - kChain));
+        }
       }
     }
   }

@@ -2,7 +2,8 @@
 kernel moe_route runs for prefill batches of the Kimi-K3 instance) against the oracle and
 against the persistent kernel that computes every score exactly (path 3), on inputs that
 drive each decision onto its hardest path: equal and nearly equal group scores (exact
-group scores from the table), more than 32 experts sharing the k-th score (the slow
+group scores from the table), 33 to 64 experts within the approximation's error band
+of the cutoff (the 64-key sort), more than 64 experts sharing the k-th score (the slow
 extraction), negative biased scores (no 32-bit keys), large biases (a wider error
 bound), and rows where every score ties."""
 import numpy as np
@@ -15,7 +16,7 @@ import parity
 
 pytestmark = pytest.mark.gpu
 
-KINDS = ("flat", "group_copy", "group_near", "negative", "large_bias", "plateau")
+KINDS = ("flat", "group_copy", "group_near", "negative", "large_bias", "plateau", "band")
 KEYS = ("packed", "counts", "offsets", "perm", "ids")
 
 
