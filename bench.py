@@ -472,7 +472,7 @@ def mufu_bound(torch, dev, T, kernel_ms, clocks):
                            f"x {sms} SMs x {mhz:.0f} MHz"}
 
 
-def workload_table(torch, mr, dev, bufs, bias3, peak_gbs):
+def workload_table(torch, mr, dev, bufs, bias3, peak_gbs, floors):
     """The measurement table of the routing configurations: small fp32 decode (8 rows),
     prefill at 16,384 and 65,536 rows (global ids and the last rank's local ids, offset
     784, count 112) and the tie-heavy 4,096-row batch (fp32 and bf16 logits, global and
@@ -505,7 +505,7 @@ def workload_table(torch, mr, dev, bufs, bias3, peak_gbs):
     b0 = torch.from_numpy(c0["bias"]).to(dev)
     o0 = mr.alloc_outputs(8, E, K, 0, dev)
     us0 = _graph_us(torch, st, [lambda: mr.route(x0, b0, out=o0, stream=st)], 200)
-    fl0 = _graph_us(torch, st, [lambda: mr.empty_kernel(mr.decode_ctas(8), stream=st)], 200)
+    fl0 = floors[mr.decode_ctas(8)]  # the decode section's floor of the same launch shape
     rows.append({"workload": "decode fp32 N(0,1)", "T": 8, "logits": "f32", "ids": "global", "l2": "warm",
                  "sets": 1, "us_per_call": round(us0, 3), "floor_us": round(fl0, 3),
                  "ratio_to_floor": round(us0 / fl0, 3)})
@@ -622,6 +622,14 @@ def main():
     if args.case is not None:
         return run_case(torch, mr, dev, args)
 
+    # Decode latency first: the empty-kernel floor it is compared with reads 0.46 us per
+    # launch until the process has run a prefill launch and then a decode graph, and about
+    # 0.66 us after (the routing calls themselves read the same in both states); the
+    # smaller floor is the one reported.
+    decode = None
+    if rank == 0 and not (args.no_decode or args.quick):
+        decode = decode_latency(torch, mr, dev)
+
     cfg = gen.cfg3(T_PREFILL)
     host_logits = np.ascontiguousarray(cfg["logits"])
     bufs = [to_dev_bf16(torch, host_logits, dev) for _ in range(NBUF)]
@@ -729,13 +737,13 @@ def main():
         e2e_ms = float(tt[0])
 
     peaks, peak_src = measured_peaks()
-    decode = gemm = layout = index = table = None
+    gemm = layout = index = table = None
     if rank == 0 and not (args.no_decode or args.quick):
-        decode = decode_latency(torch, mr, dev)
         gemm = gemm_route_latency(torch, mr, dev)
         layout = layout_timing(torch, mr, dev, outs[0], T_PREFILL, bufs=bufs, bias=bias)
         index = index_timing(torch, mr, dev, outs[0])
-        table = workload_table(torch, mr, dev, bufs, bias, peaks["hbm_gbs"])
+        table = workload_table(torch, mr, dev, bufs, bias, peaks["hbm_gbs"],
+                               dict(zip(decode["ctas"], decode["floor_us"])))
         ok = ok and mr.device_status() == 0
 
     ab = algorithmic_bytes(T_PREFILL)

@@ -407,7 +407,8 @@ int moe_route_host_release(void);
 /*
  * Measurement helper: enqueues one launch of an empty kernel with the decode kernel's
  * launch shape and attributes (a cluster of `ctas` CTAs of 256 threads, 1 <= ctas <= 16,
- * programmatic stream serialization); moe_route_decode_ctas(T) gives the shape of a
+ * the bf16 decode kernel's dynamic shared memory, programmatic stream serialization);
+ * moe_route_decode_ctas(T) gives the shape of a
  * T-row routing launch.  A cluster of more than 8 CTAs may be refused (MOE_ROUTE_E_CUDA)
  * on a GPU that cannot schedule it; the library's own launches never ask for one there.  Replayed in a
  * CUDA graph it gives the launch-latency floor that decode routing is compared with.

@@ -383,10 +383,16 @@ int decode_ctas(int T) { return decode_ctas(T, g_decode_max_ctas); }
 
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_empty() {}
 
+// The floor kernel asks for the bf16 decode kernel's shared memory, so that both run in
+// the same shared-memory configuration of the SM: with none asked for, an empty launch
+// replayed after kernels that use most of the shared memory took 0.57 us instead of 0.38.
+constexpr int kEmptySmem = DecodeSmem<DT_BF16>::total;
+
 cudaError_t launch_empty(int ctas, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, 1, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
+  cfg.dynamicSmemBytes = kEmptySmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -428,6 +434,8 @@ cudaError_t setup_decode_kernels() {
   if ((e = set_decode_smem<DT_F32, true, true>(&wide)) != cudaSuccess) return e;
   if ((e = set_decode_smem<DT_BF16, false, true>(&wide)) != cudaSuccess) return e;
   if ((e = set_decode_smem<DT_BF16, true, true>(&wide)) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(k_empty, cudaFuncAttributeMaxDynamicSharedMemorySize, kEmptySmem)) != cudaSuccess)
+    return e;
   if (cudaFuncSetAttribute(k_empty, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
     wide = false;
