@@ -173,6 +173,33 @@ def cfg_bf16_patterns(T: int, E: int = E_KIMI, off: int = 0, cnt: int = 0, seed:
                 G=G_KIMI, Kg=KG_KIMI, scale=SCALE_KIMI, off=off, cnt=cnt)
 
 
+def cfg_f32_edges(kind: str, T: int, E: int = E_KIMI, off: int = 0, cnt: int = 0) -> dict:
+    """float32 inputs at the edges of the approximate float32 scores:
+      bits   logits drawn uniformly over finite float32 bit patterns (seed 15): zeros,
+             subnormals, magnitudes where the score is 0 or 1 (many exact ties), both signs;
+      ulps   N(0,1) logits (seed 16) with 64 seeded experts per row (seed 17) at 2.5 plus
+             0..63 float steps and a zero bias, so that their biased scores differ by less
+             than the approximation's error bound.
+    """
+    bias = bias_standard(E)
+    if kind == "bits":
+        u = (raw64(15, T * E) >> np.uint64(32)).astype(np.uint32)
+        nonfinite = (u & np.uint32(0x7F800000)) == np.uint32(0x7F800000)
+        u[nonfinite] ^= np.uint32(0x40000000)
+        logits = u.view(np.float32).reshape(T, E)
+    elif kind == "ulps":
+        logits = normal_f32(16, T * E).reshape(T, E)
+        cols = (raw64(17, T * 64) % np.uint64(E)).astype(np.int64).reshape(T, 64)
+        steps = np.arange(64, dtype=np.uint32)
+        near = (np.float32(2.5).view(np.uint32) + steps).view(np.float32)
+        logits[np.arange(T)[:, None], cols] = near[None, :]
+        bias[np.unique(cols)] = 0.0
+    else:
+        raise ValueError(kind)
+    return dict(logits=np.ascontiguousarray(logits, dtype=np.float32), dtype="f32", bias=bias, T=T, E=E,
+                k=K_KIMI, G=G_KIMI, Kg=KG_KIMI, scale=SCALE_KIMI, off=off, cnt=cnt)
+
+
 def cfg_decision_edges(kind: str, T: int = 3000, E: int = E_KIMI, off: int = 0, cnt: int = 0) -> dict:
     """bf16 inputs that put every decision of the routing on its hardest path:
       flat        all logits 0 and bias 0: every score, group score and top-k value ties;

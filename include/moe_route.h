@@ -310,9 +310,11 @@ int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream
  * otherwise the persistent multi-CTA kernel), 1 = always the decode kernel (T <= 64
  * only), 2 = always the persistent kernel, 3 = always the persistent kernel and, for
  * bf16 logits with k = 16 and topk_group = 4, its variant that computes every score
- * from the exact table instead of the one that starts from approximate scores (the
- * results are identical; for comparisons).  Process-wide; for tests and benchmarks.
- * Returns the previous setting, or MOE_ROUTE_E_INVALID_ARG.
+ * from the exact table instead of the one that starts from approximate scores, 4 = the
+ * decode kernel (T <= 64 only).  Paths 3 and 4 also compute every float32 score exactly
+ * instead of starting from approximate ones (moe_route and moe_route_quant).  The
+ * results are identical on every path; the choice is for comparisons.  Process-wide;
+ * for tests and benchmarks.  Returns the previous setting, or MOE_ROUTE_E_INVALID_ARG.
  */
 int moe_route_set_path(int path);
 

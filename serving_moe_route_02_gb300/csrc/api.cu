@@ -20,6 +20,7 @@ struct DevState {
   int blocks_per_sm = 0;
   int fast_blocks_per_sm = 0;  // the approximate-score persistent kernel
   float eps_half = 0.0f;       // its measured approximation bound (route_pair.cuh)
+  float eps_f32 = -1.0f;       // route_row's float32 approximation bound
   float* stab = nullptr;  // sigmoid table for bf16 logits
   float2* etab = nullptr; // 2^(j/64) table for float32 logits
   int* err = nullptr;     // device status word
@@ -81,13 +82,15 @@ int init_device(DevState& d) {
   if (launch_sigmoid_table(d.stab, d.etab, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   // the approximation bound of the fast persistent kernel, measured into a spare word of
   // the zeroed workspace and read back (the word is zeroed again afterwards)
-  unsigned* probe = d.pw.bar + 4;
+  unsigned* probe = d.pw.bar + 4;  // and probe + 1 for the float32 bound
   if (launch_approx_err(probe, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (launch_approx_err_f32(d.etab, probe + 1, nullptr) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
-  unsigned bits = 0;
-  if (cudaMemcpy(&bits, probe, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  unsigned bits[2] = {0, 0};
+  if (cudaMemcpy(bits, probe, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (cudaMemset(probe, 0, sizeof(bits)) != cudaSuccess) return MOE_ROUTE_E_CUDA;
-  std::memcpy(&d.eps_half, &bits, sizeof(bits));
+  std::memcpy(&d.eps_half, &bits[0], sizeof(bits[0]));
+  d.eps_f32 = approx_bound_f32(bits[1]);
   d.ready.store(true, std::memory_order_release);
   return MOE_ROUTE_OK;
 }
@@ -202,9 +205,11 @@ int route_impl(const void* logits, int logits_dtype, const float* bias, int T, i
   a.NE = bins(E, k, local_count);
   a.scale = scale;
   a.eps_half = d->eps_half;
+  // paths 3 and 4 compute every float32 score exactly (for comparisons)
+  a.eps_f32 = (g_path == 3 || g_path == 4) ? -1.0f : d->eps_f32;
   const int dt = logits_dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32;
 
-  const bool decode = (g_path == 1) || (g_path == 0 && T <= 64);
+  const bool decode = (g_path == 1 || g_path == 4) || (g_path == 0 && T <= 64);
   cudaError_t ce;
   if (decode) {
     if (T > 64) return MOE_ROUTE_E_UNSUPPORTED;
@@ -333,6 +338,7 @@ int moe_route_quant(const void* logits, int logits_dtype, const float* bias, int
   a.qcodes = x_q;
   a.qscales = x_scales;
   a.qH = H;
+  a.eps_f32 = (g_path == 3 || g_path == 4) ? -1.0f : d->eps_f32;
   const int dt = logits_dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32;
   return launch_route_decode(a, dt, st) == cudaSuccess ? MOE_ROUTE_OK : MOE_ROUTE_E_CUDA;
 }
@@ -513,7 +519,7 @@ int moe_route_sigmoid(const void* x, int dtype, float* s, int n, struct CUstream
 }
 
 int moe_route_set_path(int path) {
-  if (path < 0 || path > 3) return MOE_ROUTE_E_INVALID_ARG;
+  if (path < 0 || path > 4) return MOE_ROUTE_E_INVALID_ARG;
   const int prev = g_path;
   g_path = path;
   return prev;

@@ -65,6 +65,10 @@ cudaError_t launch_route_prefill_fast(const RouteArgs& a, const PrefillWS& ws, i
                                       cudaStream_t st);
 // Writes the bits of E_half (route_pair.cuh) to *out, which must hold 0.
 cudaError_t launch_approx_err(unsigned* out, cudaStream_t st);
+// the float32 counterpart (route_row's approximate float32 scores), over all 2^32 inputs
+cudaError_t launch_approx_err_f32(const float2* etab, unsigned* out, cudaStream_t st);
+// eps_f32 from the measured maximum: the float-rounded differences' slack added
+float approx_bound_f32(unsigned measured_bits);
 // The argument checks of moe_route (status code; MOE_ROUTE_OK when the call is valid).
 int route_args_status(int T, int E, int k, int n_group, int topk_group, int off, int cnt);
 cudaError_t launch_route_prefill(const RouteArgs& a, int dtype, const PrefillWS& ws, int grid,

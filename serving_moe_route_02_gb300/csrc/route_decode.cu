@@ -18,6 +18,7 @@
 // entries of its own rows.  No global workspace and no atomics in global memory; every
 // wait is bounded.
 #include <cooperative_groups.h>
+#include <cstring>
 
 #include "launch.h"
 
@@ -354,6 +355,41 @@ __global__ void k_sigmoid(const void* x, int dtype, const float* __restrict__ ta
     s[i] = (dtype == DT_BF16) ? sig_bf16(tab, static_cast<const uint16_t*>(x)[i])
                               : sig_f32(static_cast<const float*>(x)[i], etab);
   }
+}
+
+// E_f32 = max over every float32 x (not NaN) of |0.5 tanh.approx(x / 2) + 0.5 - sig_f32(x)|,
+// the bound behind route_row's approximate float32 scores.  The difference is formed in
+// float (fma(0.5, t, 0.5) rounded, then one subtraction), so the true value is at most
+// the measured one times (1 + 2^-22) plus 2^-24, which the host adds.  For |x| > 80 the
+// exact score is 1 (x > 0: sigmoid(x) > 1 - 2^-115 rounds to 1) or below 2^-115 (x < 0),
+// so those are compared with 1 and 0 (an error of at most 2^-115, covered by the same
+// 2^-24).  Written to *out as the bits of a non-negative float; *out must start at 0.
+__global__ void k_approx_err_f32(const float2* __restrict__ etab, unsigned* out) {
+  unsigned m = 0u;
+  const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
+  for (uint64_t u = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; u < (1ull << 32); u += stride) {
+    const uint32_t bits = uint32_t(u);
+    if ((bits & 0x7F800000u) == 0x7F800000u && (bits & 0x007FFFFFu) != 0u) continue;  // NaN
+    const float x = __uint_as_float(bits);
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(__fmul_rn(x, 0.5f)));
+    const float s = fabsf(x) > 80.0f ? (x > 0.0f ? 1.0f : 0.0f) : sig_f32(x, etab);
+    const float d = fabsf(__fsub_rn(__fmaf_rn(0.5f, t, 0.5f), s));
+    m = max(m, __float_as_uint(d));
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0u) atomicMax(out, m);
+}
+
+cudaError_t launch_approx_err_f32(const float2* etab, unsigned* out, cudaStream_t st) {
+  k_approx_err_f32<<<152 * 8, 256, 0, st>>>(etab, out);
+  return cudaGetLastError();
+}
+
+float approx_bound_f32(unsigned measured_bits) {
+  float e;
+  std::memcpy(&e, &measured_bits, sizeof(e));
+  return e * (1.0f + 0x1p-22f) + 0x1p-24f;
 }
 
 cudaError_t launch_sigmoid_table(float* tab, float2* etab, cudaStream_t st) {

@@ -35,8 +35,8 @@ constexpr size_t o_prefix = o_hist + kHistBytes;
 constexpr size_t o_counts = o_prefix + kHistBytes;
 constexpr size_t o_bar = o_counts + size_t(kMaxBins) * 4;   // 2 words
 constexpr size_t o_err = o_bar + 8;                          // 1 word
-constexpr size_t o_probe = o_err + 4;                        // 1 word (set-up only)
-constexpr size_t kNoallocBytes = (o_probe + 4 + 255) / 256 * 256;
+constexpr size_t o_probe = o_err + 4;                        // 2 words (set-up only)
+constexpr size_t kNoallocBytes = (o_probe + 8 + 255) / 256 * 256;
 
 // The scratch.  In host code this name is only a stand-in for the device object; the
 // device address comes from cudaGetSymbolAddress below.
@@ -48,6 +48,7 @@ struct NoallocDev {
   int grid_max = 0;
   int grid_fast = 0;               // CTAs of the approximate-score persistent kernel
   float eps_half = 0.0f;           // its measured approximation bound
+  float eps_f32 = -1.0f;           // route_row's float32 bound
 };
 NoallocDev g_na[64];
 std::mutex g_na_mu;
@@ -68,14 +69,20 @@ int noalloc_setup(int dev, NoallocDev& d) {
   if (launch_sigmoid_table(reinterpret_cast<float*>(base + o_tab),
                            reinterpret_cast<float2*>(base + o_exp), nullptr) != cudaSuccess)
     return MOE_ROUTE_E_CUDA;
-  if (cudaMemset(base + o_bar, 0, o_probe + 4 - o_bar) != cudaSuccess) return MOE_ROUTE_E_CUDA;
+  if (cudaMemset(base + o_bar, 0, o_probe + 8 - o_bar) != cudaSuccess) return MOE_ROUTE_E_CUDA;
   if (launch_approx_err(reinterpret_cast<unsigned*>(base + o_probe), nullptr) != cudaSuccess)
+    return MOE_ROUTE_E_CUDA;
+  if (launch_approx_err_f32(reinterpret_cast<const float2*>(base + o_exp),
+                            reinterpret_cast<unsigned*>(base + o_probe + 4), nullptr) != cudaSuccess)
     return MOE_ROUTE_E_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ROUTE_E_CUDA;
   unsigned bits = 0;
   if (cudaMemcpy(&bits, base + o_probe, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ROUTE_E_CUDA;
   std::memcpy(&d.eps_half, &bits, sizeof(bits));
+  if (cudaMemcpy(&bits, base + o_probe + 4, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ROUTE_E_CUDA;
+  d.eps_f32 = approx_bound_f32(bits);
   d.base = base;
   d.grid_max = nsm * bpsm < kNoallocMaxCtas ? nsm * bpsm : kNoallocMaxCtas;
   d.grid_fast = nsm * fbpsm < kNoallocMaxCtas ? nsm * fbpsm : kNoallocMaxCtas;
@@ -145,6 +152,7 @@ extern "C" int moe_route_noalloc(const void* logits, int logits_dtype, const flo
   a.NE = NE;
   a.scale = scale;
   a.eps_half = d.eps_half;
+  a.eps_f32 = d.eps_f32;
   const int dt = logits_dtype == MOE_ROUTE_BF16 ? DT_BF16 : DT_F32;
 
   // words that must start at zero: the caller's status word and the grid barrier

@@ -55,6 +55,9 @@ struct RouteArgs {
   uint8_t* qcodes = nullptr;     // [T, qH / 2] two E2M1 codes per byte, even element low
   uint8_t* qscales = nullptr;    // [T, qH / 32] E8M0
   int qH = 0;
+  // bound on |0.5 tanh.approx(x / 2) + 0.5 - sig_f32(x)| over every float32 x, measured on
+  // the device (k_approx_err_f32); negative: float32 scores are all computed exactly
+  float eps_f32 = -1.0f;
 };
 
 // Per-warp shared scratch of the row routine.  NB = biased scores parked by the kept
@@ -128,6 +131,21 @@ __device__ __forceinline__ void sig_bf16_pair(const float* tab_lo, uint32_t v, f
   s1 = tab_lo[i2 >> 16];
 }
 
+// a - b rounded toward -infinity
+__device__ __forceinline__ float sub_rm(float a, float b) {
+  float y;
+  asm("sub.rm.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
+// Approximate biased score of a float32 logit: fma(0.5, tanh.approx(x / 2), bias + 0.5),
+// within eps_f32 + (4 + 4 max|bias|) 2^-24 of fl(sig_f32(x) + bias) (route_row).
+__device__ __forceinline__ float approx_b_f32(float x, float bias) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(__fmul_rn(x, 0.5f)));
+  return __fmaf_rn(0.5f, t, __fadd_rn(bias, 0.5f));
+}
+
 // Routes one row.  `row` points to the row's E logits (or scores) in shared memory
 // (16-byte aligned); `bias_s` to the E biases in shared memory (16-byte aligned).  All
 // 32 lanes must call it.  KC and KGC fix k and topk_group at compile time (the Kimi-K3
@@ -145,6 +163,9 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
   const float4* bq = reinterpret_cast<const float4*>(bias_s + e0);
   float b[kEPL];
   float xa1 = -INFINITY, xa2 = -INFINITY, xb1 = -INFINITY, xb2 = -INFINITY;
+  // float32 logits with a measured approximation bound take approximate scores first
+  const bool apx = DT == DT_F32 && a.eps_f32 >= 0.0f;
+  float bmag = 0.0f;  // max |bias| over this lane's experts (approximate path)
   if constexpr (DT == DT_BF16) {
     const float* tab_lo = stab - kSigLo;
     const uint2* p = reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(row) + e0);
@@ -159,6 +180,22 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
       b[4 * q + 1] = __fadd_rn(s1, bb.y);
       b[4 * q + 2] = __fadd_rn(s2, bb.z);
       b[4 * q + 3] = __fadd_rn(s3, bb.w);
+      top2_pair(xa1, xa2, b[4 * q + 0], b[4 * q + 1]);
+      top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
+    }
+  } else if (apx) {
+    // float32 logits: approximate biased scores (one tanh.approx each), exact ones below
+    // only for the experts a decision can depend on
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(row) + e0);
+#pragma unroll
+    for (int q = 0; q < kEPL / 4; ++q) {
+      const float4 v = p[q];
+      const float4 bb = bq[q];
+      b[4 * q + 0] = approx_b_f32(v.x, bb.x);
+      b[4 * q + 1] = approx_b_f32(v.y, bb.y);
+      b[4 * q + 2] = approx_b_f32(v.z, bb.z);
+      b[4 * q + 3] = approx_b_f32(v.w, bb.w);
+      bmag = fmaxf(fmaxf(bmag, fmaxf(fabsf(bb.x), fabsf(bb.y))), fmaxf(fabsf(bb.z), fabsf(bb.w)));
       top2_pair(xa1, xa2, b[4 * q + 0], b[4 * q + 1]);
       top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
     }
@@ -179,8 +216,45 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
       top2_pair(xb1, xb2, b[4 * q + 2], b[4 * q + 3]);
     }
   }
-  const float lm1 = fmaxf(xa1, xb1);
-  const float lm2 = fmax3(fminf(xa1, xb1), xa2, xb2);
+  float lm1 = fmaxf(xa1, xb1);
+  float lm2 = fmax3(fminf(xa1, xb1), xa2, xb2);
+  // exact biased scores of this lane's experts whose bits are set in m, two at a time;
+  // f(i, b) is called for each
+  auto exact_f32 = [&](uint32_t m, auto&& f) {
+    const float* xr = static_cast<const float*>(row) + e0;
+    while (m) {
+      const int i0 = __ffs(m) - 1;
+      m &= m - 1u;
+      const int i1 = m ? __ffs(m) - 1 : i0;
+      m &= m - 1u;
+      const float v0 = __fadd_rn(sig_f32(xr[i0], a.etab), bias_s[e0 + i0]);
+      const float v1 = __fadd_rn(sig_f32(xr[i1], a.etab), bias_s[e0 + i1]);
+      f(i0, v0);
+      if (i1 != i0) f(i1, v1);
+    }
+  };
+  float eps = 0.0f;
+  if (apx) {
+    // |approximate - exact| <= eps for every expert of the row: the measured bound plus the
+    // roundings of bias + 0.5, of the fma and of the exact sum (each within 2^-24 of its
+    // magnitude, at most 1 + max|bias|), with slack for the float arithmetic here
+    const float B = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(bmag)));
+    eps = (a.eps_f32 + (4.0f + 4.0f * B) * 0x1p-24f) * (1.0f + 0x1p-20f);
+    // the lane's exact top two: two experts have approximate scores >= lm2, so the exact
+    // second largest is >= lm2 - eps, and either of the two has an approximate score of
+    // at least lm2 - 2 eps
+    const float thr = sub_rm(lm2, 2.0f * eps);
+    uint32_t cm = 0;
+#pragma unroll
+    for (int i = 0; i < kEPL; ++i) cm |= (b[i] >= thr) ? (1u << i) : 0u;
+    float e1 = -INFINITY, e2 = -INFINITY;
+    exact_f32(cm, [&](int, float e) {
+      e2 = fmaxf(e2, fminf(e1, e));
+      e1 = fmaxf(e1, e);
+    });
+    lm1 = e1;
+    lm2 = e2;
+  }
 
   // ---- a3: group score = sum of the group's two largest b (4-lane merge of top-2 lists)
   float gm1 = lm1, gm2 = lm2;
@@ -256,8 +330,21 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
 
   uint32_t smask = 0;
   if (kept) {
+    if (apx) {
+      // survivors have exact b >= tau0, so approximate b >= tau0 - eps: those get their
+      // exact score, parked over the approximate one (the others stay below tau0)
+      const float thr = sub_rm(tau0, eps);
+      uint32_t dm = 0;
 #pragma unroll
-    for (int i = 0; i < kEPL; ++i) smask |= (b[i] >= tau0) ? (1u << i) : 0u;
+      for (int i = 0; i < kEPL; ++i) dm |= (b[i] >= thr) ? (1u << i) : 0u;
+      exact_f32(dm, [&](int i, float e) {
+        ws.b[ki * kEPL + i] = e;
+        smask |= (e >= tau0) ? (1u << i) : 0u;
+      });
+    } else {
+#pragma unroll
+      for (int i = 0; i < kEPL; ++i) smask |= (b[i] >= tau0) ? (1u << i) : 0u;
+    }
   }
   // inclusive prefix of the per-lane counts c (0..28, five bits) by bit slices: five
   // independent ballots instead of a five-step shuffle chain

@@ -66,7 +66,9 @@ def test_sigmoid_f32_within_1ulp(mr):
     """float32 logits: within one ulp of the oracle everywhere, equal almost everywhere."""
     x = np.concatenate([gen.uniform_f32(11, 1 << 20, -40.0, 40.0), gen.normal_f32(12, 1 << 20),
                         gen.normal_f32(13, 1 << 18) * np.float32(1e-4),
-                        gen.uniform_f32(14, 1 << 16, -104.0, -80.0)]).astype(np.float32)
+                        gen.uniform_f32(14, 1 << 16, -104.0, -80.0),
+                        gen.uniform_f32(18, 1 << 16, 60.0, 200.0),
+                        gen.cfg_f32_edges("bits", 64)["logits"].ravel()]).astype(np.float32)
     got = mr.sigmoid(torch.from_numpy(x).cuda()).cpu().numpy()
     want = oracle.sigmoid(x, "f32")
     d = np.abs(got.view(np.int32).astype(np.int64) - want.view(np.int32).astype(np.int64))
@@ -138,6 +140,30 @@ def test_every_bf16_magnitude(mr, T, path, off, cnt):
     2^-26 and above 112, both signs) reach the clamped score-table lookups of the row
     routine on both paths; many exact ties in b."""
     check(mr, gen.cfg_bf16_patterns(T, off=off, cnt=cnt), exact=True, path=path)
+
+
+@pytest.mark.parametrize("T,paths", [(8, (1, 4)), (64, (1, 4)), (3000, (2, 3))])
+@pytest.mark.parametrize("kind", ["cfg0", "cfg4", "bits", "ulps"])
+def test_f32_approximate_scores_agree(mr, T, paths, kind):
+    """float32 logits: routing that starts from approximate scores (paths 1 and 2) equals
+    routing that computes every score exactly (paths 4 and 3), on the decode and the
+    persistent kernel, including logits where the score saturates and experts whose
+    scores differ by less than the approximation's error bound."""
+    if kind == "cfg0":
+        cfg = dict(gen.cfg0(max(T, 8)))
+    elif kind == "cfg4":
+        cfg = gen.cfg4(T=T, off=336, cnt=112)
+    else:
+        cfg = gen.cfg_f32_edges(kind, T)
+    a = run_gpu(mr, cfg, path=paths[0])
+    b = run_gpu(mr, cfg, path=paths[1])
+    for key in ("packed", "counts", "offsets", "perm", "ids"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("kind", ["bits", "ulps"])
+def test_f32_edges_oracle(mr, kind):
+    check(mr, gen.cfg_f32_edges(kind, 3000, off=784, cnt=112), exact=False)
 
 
 def test_t_zero(mr):
