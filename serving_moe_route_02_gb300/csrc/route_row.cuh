@@ -14,8 +14,8 @@
 // one per lane in expert-id order with 32-bit keys (b relative to tau0, then position,
 // so exact ties go to the lower id); a survivor's slot is the number of larger keys.
 // When the key range does not allow such keys, k rounds of a warp maximum pick the
-// slots.  If more than 32 survive, a slower exact path extracts the k winners from
-// per-lane maxima.  Rank counting reads the pool and the keys from shared memory, so
+// slots.  33 to 64 survivors are ranked the same way, two per lane; beyond that a
+// slower exact path extracts the k winners from per-lane maxima.  Rank counting reads the pool and the keys from shared memory, so
 // its latency is a few loads instead of a chain of shuffles.
 #pragma once
 #include "common.cuh"
@@ -66,8 +66,8 @@ template <int NB>
 struct WarpScratchT {
   float b[NB];            // biased scores of the kept lanes (kept lane i at [28 i, 28 i + 28))
   float pool[32];         // threshold pool
-  uint32_t skey[32];      // survivor keys
-  int32_t sid[32];        // survivor expert ids
+  uint32_t skey[64];      // survivor keys
+  int32_t sid[64];        // survivor expert ids
   int32_t slot_id[kMaxK]; // expert id of each slot
 };
 using WarpScratch = WarpScratchT<kEPL * 32>;
@@ -361,10 +361,14 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
 
   // composite 32-bit keys (b, position) need tau0 > 0 and survivors within 2^26 float
   // steps of it (b >= 0 there, so float bits order like the values)
-  bool keys32 = false;
-  if (total <= 32 && tau0 > 0.0f) {
+  bool keys32 = false, keys64 = false;
+  if (total <= 64 && tau0 > 0.0f) {
     const uint32_t bmax = __reduce_max_sync(FULL, kept ? __float_as_uint(lm1) : 0u);
-    keys32 = (bmax - __float_as_uint(tau0)) < (1u << 26);
+    keys32 = total <= 32 && (bmax - __float_as_uint(tau0)) < (1u << 26);
+    // float32 rows only: compiled into the bf16 and score instances, the 64-key ranking
+    // cost their common rows 0.05-0.3 us per call (decode and contraction + routing)
+    if constexpr (DT == DT_F32)
+      keys64 = total > 32 && (bmax - __float_as_uint(tau0)) < (1u << 26) - 1u;  // 6 position bits
   }
 
   if (total <= 32) {
@@ -419,6 +423,33 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
         }
       }
     }
+  } else if (DT == DT_F32 && keys64) {
+    // 33 to 64 survivors (ties or near ties around tau0): two per lane, the same keys with
+    // 6 position bits, each ranked against all 64 (positions past `total` hold 0)
+    if (lane + 32 >= total) ws.skey[lane + 32] = 0u;
+    int pos = incl - c;
+    while (smask) {
+      const int i = __ffs(smask) - 1;
+      smask &= smask - 1u;
+      const float bv = ws.b[ki * kEPL + i];
+      ws.skey[pos] = ((__float_as_uint(bv) - __float_as_uint(tau0) + 1u) << 6) | uint32_t(63 - pos);
+      ws.sid[pos] = e0 + i;
+      ++pos;
+    }
+    __syncwarp();
+    const uint32_t key0 = ws.skey[lane], key1 = ws.skey[lane + 32];
+    const uint4* k4 = reinterpret_cast<const uint4*>(ws.skey);
+    int r0 = 0, r1 = 0, q0 = 0, q1 = 0;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const uint4 u = k4[q];
+      r0 += int(u.x > key0) + int(u.y > key0);
+      r1 += int(u.z > key0) + int(u.w > key0);
+      q0 += int(u.x > key1) + int(u.y > key1);
+      q1 += int(u.z > key1) + int(u.w > key1);
+    }
+    if (r0 + r1 < k) ws.slot_id[r0 + r1] = ws.sid[lane];  // lane < 32 < total
+    if (lane + 32 < total && q0 + q1 < k) ws.slot_id[q0 + q1] = ws.sid[lane + 32];
   } else {
     // exact slow path: k rounds of (warp max over lane maxima), winner lane rescans
     uint32_t taken = 0;
