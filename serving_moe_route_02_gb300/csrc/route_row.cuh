@@ -457,12 +457,20 @@ __device__ __forceinline__ SlotOut route_row(const void* row, const float* bias_
       bk = 0u;
       bi = -1;
       if (!kept) return;
-      for (int i = 0; i < kEPL; ++i) {
-        if (taken & (1u << i)) continue;
-        const uint32_t kk = fkey(ws.b[ki * kEPL + i]);
-        if (kk > bk) {
-          bk = kk;
-          bi = i;
+      // the lane's 28 parked scores in seven 16-byte loads, all in flight at once
+      const float4* p = reinterpret_cast<const float4*>(ws.b + ki * kEPL);
+#pragma unroll
+      for (int q = 0; q < kEPL / 4; ++q) {
+        const float4 u = p[q];
+        const float v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int i = 4 * q + r;
+          const uint32_t kk = ((taken >> i) & 1u) ? 0u : fkey(v[r]);
+          if (kk > bk) {
+            bk = kk;
+            bi = i;
+          }
         }
       }
     };
