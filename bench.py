@@ -230,7 +230,10 @@ def decode_latency(torch, mr, dev, reps=200, replays=10):
     fused route+quant launch (the same routing plus the MXFP4 quantisation of the batch's
     bf16 activations [T, 7168])."""
     res = {"T": [], "ctas": [], "us_per_call": [], "floor_us": [], "ratio_to_floor": [],
-           "route_quant_us_per_call": []}
+           "route_quant_us_per_call": [],
+           "floor_kernel": "empty kernel with the routing launch's cluster shape, programmatic "
+                           "stream serialization and 118 KB of dynamic shared memory, replayed "
+                           "the same way, measured before the process runs any prefill launch"}
     st = torch.cuda.Stream(device=dev)
     for T in (8, 16, 24, 32, 64):
         cfg = gen.cfg1(T)
